@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 attention sublayer.
+
+One step is one pass of the path over one batch of synthetic inputs resident
+in HBM: the fused Q/K/V projection plus attention of the sublayer workload
+(fp32 storage, TF32 tensor-core products, x [8,512,512], Wqkv [512,1536],
+H=8, D=64, non-causal), through the C ABI (la_layer_attn).  The line also
+reports, each timed the same way, the other workloads of the path: fp32
+causal attention B=8 H=8 S=2048 D=64 (with and without key padding), bf16
+causal attention B=4 H=16 S=4096 D=128, the chunked 100k-token mode (bf16
+causal B=2 H=16 S=100000 D=64, windows of 4096 against a growing cache) and
+the small fp32 case B=1 H=2 S=128 D=64.
+
+FLOPs are algorithmic (useful work only): 2*rows*d*3d for the projection and
+4*D per (query, visible key) pair per head for attention.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: one process per GPU under torchrun; every rank runs the same
+workload on its own GPU (independent replicas: the path has no exchange
+step), the time is the max over ranks and the value counts all ranks' work.
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and ms per layer at 1 GB300; % of tensor-pipe peak"
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 / BF16 tensor rates
+L2_FLUSH_BYTES = 256 << 20           # larger than the 129 MB L2
+
+HEADLINE = dict(B=8, S=512, d_model=512, H=8)
+HEADLINE_NAME = "attention sublayer fp32 (TF32 MMA) B=8 S=512 d_model=512 H=8 D=64 non-causal: qkv_proj + attention"
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _tensor_peak(dtype, peaks, sustained=False):
+    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return bf16 * NOMINAL_TF32_OVER_BF16 if dtype == torch.float32 else bf16
+
+
+def _source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "layer_attn_fwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel, workload, files):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[f"{kernel} | {workload}"]
+        return e["bytes_per_launch"] if e["source_sha"] == _source_sha(files) else None
+    except Exception:
+        return None
+
+
+class Clocks:
+    """Sample SM clocks and throttle reasons with nvidia-smi while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        load = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized():
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _time_steps(step, K, W, flush, stream, barrier):
+    """W untimed steps, then K steps each bracketed by CUDA events on `stream`
+    with an L2 flush (not timed) between them.  Returns total device ms."""
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(K):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            step()
+            e.record(stream)
+            evs.append((s, e))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in evs)
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    from layer_attn_fwd_gb300 import api, build, flops, inputs
+
+    ws_n, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    build.build()
+    api.load()
+    peaks = _peaks()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    K, W = args.steps, args.warmup
+
+    # ---- headline: the sublayer -------------------------------------------
+    B, S, dm, H = HEADLINE["B"], HEADLINE["S"], HEADLINE["d_model"], HEADLINE["H"]
+    D = dm // H
+    x_h, W_h, b_h = inputs.layer_inputs(B, S, dm, torch.float32, seed=0)
+    x, Wq, bq = x_h.to(dev), W_h.to(dev), b_h.to(dev)
+    o = torch.empty_like(x)
+    ws_layer = api.workspace_size(api.LA_OP_LAYER_ATTN, B, H, S, S, D, torch.float32)
+    ws = torch.empty(ws_layer, dtype=torch.uint8, device=dev)
+    qkv_bytes = 3 * ((B * S * dm * 4 + 255) // 256 * 256)
+    launches_per_step = 2 + (1 if ws_layer > qkv_bytes else 0)
+    fl_proj = flops.proj_flops(B, S, dm)
+    fl_attn = flops.attn_flops(B, H, S, S, D, False)
+    fl_step = fl_proj + fl_attn
+
+    def layer_step():
+        api.layer_attn(x, Wq, bq, H, out=o, workspace=ws, stream=stream)
+
+    with Clocks(local) as clk:
+        ms_total = _time_steps(layer_step, K, W, flush, stream, barrier)
+    clocks = clk.summary()
+    st = api.get_last_error(stream)
+    if st != api.LA_OK:
+        raise RuntimeError(f"device status after the timed steps: {api.status_string(st)}")
+    ms_max = max_over_ranks(ms_total, dist, dev)
+    ms_step = ms_max / K
+    value = fl_step * K * ws_n / (ms_max * 1e-3) / 1e12
+
+    # ---- the two kernels of the step, each timed alone ------------------------
+    q = torch.empty(B, H, S, D, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty_like(q)
+    oh = torch.empty_like(q)
+    api.qkv_proj(x, Wq, bq, H, out=(q, k, v), stream=stream)
+    ms_proj = _time_steps(lambda: api.qkv_proj(x, Wq, bq, H, out=(q, k, v), stream=stream), K, W, flush, stream,
+                          barrier) / K
+    ms_att = _time_steps(lambda: api.attn_fwd(q, k, v, out=oh, stream=stream), K, W, flush, stream, barrier) / K
+    per_kernel = {
+        "qkv_proj": {"ms": ms_proj, "tflops": fl_proj / (ms_proj * 1e-3) / 1e12},
+        "attn_fwd": {"ms": ms_att, "tflops": fl_attn / (ms_att * 1e-3) / 1e12},
+    }
+    dom = "attn_fwd" if ms_att >= ms_proj else "qkv_proj"
+    peak_tf32 = _tensor_peak(torch.float32, peaks)
+    src = ["la_attn.cu", "la_device.cuh"] if dom == "attn_fwd" else ["la_proj.cu", "la_device.cuh"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(per_kernel[dom]["tflops"], 2),
+                "peak": round(peak_tf32, 1), "unit": "TFLOP/s",
+                "frac": round(per_kernel[dom]["tflops"] / peak_tf32, 4),
+                "traffic": _traffic(dom, "sublayer fp32 B8 S512 d512", src),
+                "peak_note": f"TF32 = {peaks['source']} bf16 burst x nominal 1.1/2.25"}
+
+    # ---- end to end through the public API, host buffers -------------------------
+    x_pin = x_h.pin_memory()
+    o_pin = torch.empty_like(x_h).pin_memory()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x.copy_(x_pin, non_blocking=True)
+            api.layer_attn(x, Wq, bq, H, out=o, workspace=ws, stream=stream)
+            o_pin.copy_(o, non_blocking=True)
+
+    ms_e2e = max_over_ranks(_time_steps(e2e_step, K, W, flush, stream, barrier), dist, dev)
+    e2e = {"value": round(fl_step * K * ws_n / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+           "ms_per_step": round(ms_e2e / K, 4), "h2d_bytes_per_step": x_h.numel() * 4,
+           "d2h_bytes_per_step": x_h.numel() * 4}
+
+    # ---- the other workloads of the path --------------------------------------------
+    workloads = {}
+    if not args.headline_only:
+        workloads = other_workloads(args, dev, stream, flush, barrier, peaks)
+
+    # ---- CPU baseline: the oracle on the host cores (rank 0, N=1 only) ------------------
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu:
+        cpu = cpu_baseline_sample(x_h, W_h, b_h, H, seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws_n, "steps": K, "warmup": W,
+            "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": HEADLINE_NAME, "math": "TF32 tensor-core products, fp32 accumulate and softmax",
+                       "l2": "flushed between timed steps (256 MB write)", "parallelism": f"replicas x{ws_n}",
+                       "batch": B, "seq_len": S, "d_model": dm, "heads": H},
+            "frac_of_tensor_peak": round(value / ws_n / peak_tf32, 4),
+            "roofline": roofline, "per_kernel": per_kernel, "e2e": e2e,
+            "gpu_launches": launches_per_step * K, "clocks": clocks, "cpu_baseline": cpu,
+            "workloads": workloads, "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def other_workloads(args, dev, stream, flush, barrier, peaks):
+    from layer_attn_fwd_gb300 import api, flops, inputs
+
+    res = {}
+    Kx = max(3, min(args.steps, 20))
+
+    def attn_case(name, B, H, S, D, dt, causal, padded=False):
+        q, k, v = (t.to(dev) for t in inputs.attn_inputs(B, H, S, S, D, dt, seed=0))
+        kv = inputs.padding_kv_len(B, S) if padded else None
+        kl = kv.to(dev) if kv is not None else None
+        o = torch.empty_like(q)
+        n = api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, dt)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+        ms = _time_steps(lambda: api.attn_fwd(q, k, v, causal=causal, kv_len=kl, out=o, workspace=ws,
+                                              stream=stream), Kx, 3, flush, stream, barrier) / Kx
+        fl = flops.attn_flops(B, H, S, S, D, causal, kv)
+        tf = fl / (ms * 1e-3) / 1e12
+        pk = _tensor_peak(dt, peaks)
+        res[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / pk, 4),
+                     "gflop": round(fl / 1e9, 3)}
+        del q, k, v, o, ws
+
+    attn_case("fp32 causal B8 H8 S2048 D64", 8, 8, 2048, 64, torch.float32, True)
+    attn_case("fp32 causal B8 H8 S2048 D64, last 25% keys padded for half the batch", 8, 8, 2048, 64,
+              torch.float32, True, padded=True)
+    attn_case("bf16 causal B4 H16 S4096 D128", 4, 16, 4096, 128, torch.bfloat16, True)
+    attn_case("fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False)
+
+    # chunked 100k-token mode: 25 windows of 4096 (the last 1696) per step
+    B, H, S, D, C = 2, 16, 100000, 64, 4096
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=0)
+    wins = inputs.chunk_bounds(S, C)
+    qs = [q[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
+    ks = [k[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
+    vs = [v[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
+    del q, k, v
+    cache = api.KVCache(B, H, S, D, torch.bfloat16, device=dev)
+    outs = [torch.empty_like(t) for t in qs]
+    n = api.workspace_size(api.LA_OP_ATTN_CHUNKED, B, H, C, S, D, torch.bfloat16)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+
+    def chunked_step():
+        cache.reset()
+        for i in range(len(wins)):
+            api.attn_chunked(qs[i], ks[i], vs[i], cache, out=outs[i], workspace=ws, stream=stream)
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    ms = _time_steps(chunked_step, 3, 1, flush, stream, barrier) / 3
+    fl = flops.attn_flops(B, H, S, S, D, True)
+    tf = fl / (ms * 1e-3) / 1e12
+    res["chunked bf16 causal B2 H16 S100000 D64, windows of 4096"] = {
+        "ms": round(ms, 3), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / _tensor_peak(torch.bfloat16, peaks), 4),
+        "gflop": round(fl / 1e9, 1), "windows": len(wins), "workspace_bytes": n,
+        "peak_device_bytes": torch.cuda.max_memory_allocated(dev)}
+    st = api.get_last_error(stream)
+    if st != api.LA_OK:
+        raise RuntimeError(f"device status after the extra workloads: {api.status_string(st)}")
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle
+# ---------------------------------------------------------------------------
+def cpu_baseline_sample(x_h, W_h, b_h, H, seconds=20.0):
+    """Time the fp64 oracle on a bounded sample of the sublayer workload: the
+    first batch entries, as many as fit in about `seconds` of CPU work."""
+    import oracle
+    from layer_attn_fwd_gb300 import flops
+
+    S, dm = x_h.shape[1], x_h.shape[2]
+    D = dm // H
+    done_b, t_total = 0, 0.0
+    while done_b < x_h.shape[0] and t_total < seconds:
+        t0 = time.perf_counter()
+        oracle.layer_attn(x_h[done_b:done_b + 1].contiguous(), W_h, b_h, H)
+        t_total += time.perf_counter() - t0
+        done_b += 1
+    fl = done_b * (flops.proj_flops(1, S, dm) + flops.attn_flops(1, H, S, S, D, False))
+    return {"value": round(fl / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done_b} of {x_h.shape[0]} batch entries of the sublayer workload ({t_total:.1f} s, fp64, OpenMP)"}
+
+
+def run_reference(args):
+    ws_n, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from layer_attn_fwd_gb300 import flops, inputs
+
+    B, S, dm, H = HEADLINE["B"], HEADLINE["S"], HEADLINE["d_model"], HEADLINE["H"]
+    D = dm // H
+    x, W, b = inputs.layer_inputs(B, S, dm, torch.float32, seed=0)
+    oracle.build()
+    # one step = the oracle on one batch entry of the workload (a bounded sample)
+    xs = [x[i:i + 1].contiguous() for i in range(B)]
+    fl = flops.proj_flops(1, S, dm) + flops.attn_flops(1, H, S, S, D, False)
+    for i in range(args.warmup):
+        oracle.layer_attn(xs[i % B], W, b, H)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.layer_attn(xs[i % B], W, b, H)
+    t = time.perf_counter() - t0
+    value = fl * args.steps / t / 1e12
+    cores = oracle.num_threads()
+    sample = f"one of the {B} batch entries per step (x [1,{S},{dm}]), fp64, OpenMP"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE_NAME, "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * layerattn.h -- C ABI of the GB300 (sm_103a) attention-sublayer library
+ * liblayerattn.so.
+ *
+ * The operation is the attention step of a transformer inference layer,
+ * O = softmax(Q K^T * scale) V ("Shape-Aware Attention", section Inspiration,
+ * the attention equation), computed by online softmax over key/value tiles so
+ * that the [B, H, S_q, S_kv] score matrix never exists ("GPU Kernel for a
+ * Transformer Layer", section What we learned), with causal masking ("GPU
+ * Kernel for a Transformer Layer", section How we built it), an optional key
+ * padding mask, a fused Q/K/V projection feeding it and a chunked
+ * long-context mode that streams query windows against a growing key/value
+ * cache ("Roofline", sections What it does and How we built it).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned, to contiguous row-major tensors.  The library allocates no
+ *    device memory on any call; scratch comes from the caller's workspace
+ *    `ws` of `ws_bytes` bytes (size it with la_workspace_size()).
+ *  - q, k, v, o are head-major [B, H, S, D] unless stated otherwise.
+ *  - Element types: LA_F32 (fp32 storage; the products run on the tensor
+ *    cores in TF32 with fp32 accumulation), LA_BF16 and LA_F16 (half-precision
+ *    storage; fp32 softmax statistics and fp32 accumulation).  Outputs have
+ *    the input element type, rounded to nearest-even.
+ *  - Supported head dimension: D in {64, 128}.  Any other D returns
+ *    LA_ERR_UNSUPPORTED; there is no fallback path.
+ *  - Causal masking aligns query rows to the END of the key range: query row
+ *    i (0 <= i < S_q) is absolute position S_kv - S_q + i and sees keys
+ *    j <= S_kv - S_q + i.  With S_q == S_kv this is ordinary causal attention.
+ *  - kv_len (nullable) is a device array of B int32: keys j >= kv_len[b] of
+ *    batch entry b are masked out (key padding).  Values above S_kv are
+ *    clamped to S_kv.
+ *  - A query row with no visible key yields a zero output row.
+ *  - scale must be positive and finite (usually 1/sqrt(D)).
+ *  - Every call is asynchronous on the caller's stream `st` (a cudaStream_t;
+ *    NULL is the legacy default stream).  Arguments are validated on the
+ *    host before any launch; an invalid call launches nothing and returns a
+ *    status.  Device-side failures (a bounded wait that ran out) are latched
+ *    in a device error word and reported by la_get_last_error().
+ *  - Nothing throws, aborts, prints or traps across this boundary.
+ *  - Inputs must be finite.  Masked keys are excluded by their weight, so
+ *    padding keys must hold finite values.
+ */
+#ifndef LAYERATTN_H
+#define LAYERATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID = 1,      /* bad pointer, size, alignment or parameter  */
+    LA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (D, dtype)       */
+    LA_ERR_WORKSPACE = 3,    /* ws smaller than the call needs             */
+    LA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed       */
+    LA_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out         */
+    LA_ERR_INTERNAL = 6      /* a device-side consistency check failed     */
+} la_status;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1, LA_F16 = 2 } la_dtype;
+
+/* Operation codes for la_workspace_size(). */
+typedef enum { LA_OP_ATTN_FWD = 0, LA_OP_ATTN_CHUNKED = 1, LA_OP_LAYER_ATTN = 2 } la_op;
+
+/*
+ * Growing key/value cache for the chunked mode.  k and v are caller-owned
+ * device buffers [B, H, S_max, D] of element type `dtype`; positions
+ * [0, len) hold valid keys/values.  la_attn_chunked() appends to it and
+ * advances `len` on the host struct.
+ */
+typedef struct {
+    void *k;
+    void *v;
+    int B, H, D, S_max, len;
+    la_dtype dtype;
+} la_kv_cache;
+
+/*
+ * Fused Q/K/V projection ("Roofline", sections What it does and How we built
+ * it: one product x.Wqkv instead of three).
+ *   x     [B, S, d_model]            input activations
+ *   Wqkv  [d_model, 3*d_model]       columns: the Q block, the K block, the V
+ *                                    block; inside each block head h owns
+ *                                    columns h*D .. h*D+D-1 (D = d_model / H)
+ *   bqkv  [3*d_model] or NULL        bias, same column order
+ *   q,k,v [B, H, S, D] outputs       y = x.Wqkv + bqkv split per head; q is
+ *                                    further multiplied by q_scale
+ * d_model must be H*D with D in {64, 128}.  S >= 0 (S == 0 is a no-op).
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED or LA_ERR_CUDA.
+ */
+la_status la_qkv_proj(const void *x, const void *Wqkv, const void *bqkv,
+                      void *q, void *k, void *v,
+                      int B, int S, int d_model, int H, float q_scale,
+                      la_dtype dt, la_stream_t st);
+
+/*
+ * Attention forward ("Shape-Aware Attention", section Inspiration, the
+ * attention equation; online softmax per "GPU Kernel for a Transformer
+ * Layer", section What we learned).
+ *   q [B, H, S_q, D]; k, v [B, H, S_kv, D]; o [B, H, S_q, D] output.
+ *   causal, scale, kv_len: see the conventions above.
+ *   ws, ws_bytes: optional workspace.  With at least
+ *     la_workspace_size(LA_OP_ATTN_FWD, ...) bytes the call may split long
+ *     key ranges across thread blocks and merge the partial results
+ *     (split-KV); with less (or NULL) it runs unsplit.  Results agree to
+ *     rounding either way.
+ * S_q == 0 is a no-op; S_kv == 0 writes zero rows.  q and o may be NULL
+ * only when S_q == 0, k and v only when S_kv == 0.
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED or LA_ERR_CUDA.
+ */
+la_status la_attn_fwd(const void *q, const void *k, const void *v, void *o,
+                      int B, int H, int S_q, int S_kv, int D, int causal, float scale,
+                      const int32_t *kv_len, la_dtype dt,
+                      void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
+ * One window of the chunked long-context mode ("Roofline", sections What it
+ * does and How we built it: bounded-memory query windows against a growing
+ * key/value cache).  The window's keys and values
+ *   k_chunk, v_chunk [B, H, chunk, D]
+ * are appended to the cache at positions [len, len+chunk), then the window's
+ * queries q_chunk [B, H, chunk, D] attend to cache positions [0, len+chunk)
+ * (causal rows aligned to the end), writing o_chunk [B, H, chunk, D], and
+ * cache->len grows by chunk.  Calling it window after window over a sequence
+ * gives the same result as attending the whole sequence at once.
+ * cache->len + chunk must not exceed cache->S_max; cache->dtype, B, H and D
+ * describe all five tensors.  ws: as for la_attn_fwd, sized with
+ * la_workspace_size(LA_OP_ATTN_CHUNKED, B, H, chunk, S_max, D, dtype).
+ * On any non-OK status cache->len is unchanged.
+ */
+la_status la_attn_chunked(const void *q_chunk, const void *k_chunk, const void *v_chunk,
+                          la_kv_cache *cache, void *o_chunk, int chunk, int causal,
+                          float scale, void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
+ * The attention sublayer as a layer runs it: la_qkv_proj (q_scale 1), then
+ * attention per head with scale 1/sqrt(D), heads merged in the store:
+ *   x [B, S, d_model], Wqkv [d_model, 3*d_model], bqkv [3*d_model] or NULL,
+ *   o [B, S, d_model] with head h in columns h*D .. h*D+D-1.
+ * The output projection is not applied.  ws must hold at least
+ * la_workspace_size(LA_OP_LAYER_ATTN, B, H, S, S, d_model / H, dt) bytes
+ * (the head-major q, k, v); otherwise LA_ERR_WORKSPACE.
+ */
+la_status la_layer_attn(const void *x, const void *Wqkv, const void *bqkv, void *o,
+                        int B, int S, int d_model, int H, int causal,
+                        const int32_t *kv_len, la_dtype dt,
+                        void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
+ * Workspace bytes an operation wants (0 if none).  op is an la_op; the
+ * remaining arguments are those of the call (for LA_OP_ATTN_CHUNKED pass
+ * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN pass
+ * S_q = S_kv = S).  Returns (size_t)-1 for invalid arguments.  Host only;
+ * touches no device.
+ */
+size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt);
+
+/*
+ * Synchronises `st`, then reports and clears the device error word of the
+ * current device: LA_ERR_TIMEOUT if a kernel's bounded wait ran out since
+ * the last query, LA_ERR_INTERNAL if a device consistency check failed,
+ * LA_ERR_CUDA if the stream itself reports an error, else LA_OK.
+ */
+la_status la_get_last_error(la_stream_t st);
+
+/* Static, human-readable name of a status. */
+const char *la_status_string(la_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYERATTN_H */

@@ -1,0 +1,206 @@
+"""Thin ctypes binding of liblayerattn.so (declared in include/layerattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  Tensors are torch CUDA tensors (PyTorch supplies device memory and
+streams); calls go onto ``torch.cuda.current_stream()``.  Workspaces are
+allocated here with torch when the caller passes none; the library itself
+never allocates.  A missing library raises ``RuntimeError``; there is no CPU
+or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "liblayerattn.so")
+
+LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_INTERNAL = range(7)
+LA_F32, LA_BF16, LA_F16 = 0, 1, 2
+LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN = 0, 1, 2
+
+_DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16, torch.float16: LA_F16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LayerAttnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+class la_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("B", ctypes.c_int), ("H", ctypes.c_int),
+                ("D", ctypes.c_int), ("S_max", ctypes.c_int), ("len", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+def load(path: str | None = None):
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"liblayerattn.so not built ({path}); run layer_attn_fwd_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.la_qkv_proj.argtypes = [P, P, P, P, P, P, I, I, I, I, F, I, P]
+        lib.la_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, I, P, Z, P]
+        lib.la_attn_chunked.argtypes = [P, P, P, ctypes.POINTER(la_kv_cache), P, I, I, F, P, Z, P]
+        lib.la_layer_attn.argtypes = [P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
+        lib.la_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.la_workspace_size.restype = Z
+        lib.la_get_last_error.argtypes = [P]
+        lib.la_status_string.argtypes = [I]
+        lib.la_status_string.restype = ctypes.c_char_p
+        for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_get_last_error"):
+            getattr(lib, name).restype = I
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().la_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != LA_OK:
+        raise LayerAttnError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _need(t, name, dev=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dev and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(op, B, H, S_q, S_kv, D, dtype) -> int:
+    n = load().la_workspace_size(int(op), B, H, S_q, S_kv, D, _DT[dtype])
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("workspace_size: invalid arguments")
+    return int(n)
+
+
+def _workspace(nbytes, device, ws):
+    if ws is not None:
+        return ws
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def qkv_proj(x, Wqkv, bqkv, H, q_scale=1.0, out=None, stream=None):
+    """x [B,S,d], Wqkv [d,3d], bqkv [3d] or None -> q, k, v [B,H,S,D]."""
+    for t, n in ((x, "x"), (Wqkv, "Wqkv")):
+        _need(t, n)
+    if bqkv is not None:
+        _need(bqkv, "bqkv")
+    B, S, dm = x.shape
+    D = dm // H if H > 0 else 0
+    if out is None:
+        out = tuple(torch.empty(B, H, S, D, dtype=x.dtype, device=x.device) for _ in range(3))
+    q, k, v = out
+    _check(load().la_qkv_proj(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(q), _ptr(k), _ptr(v), B, S, dm, H,
+                              float(q_scale), _dt(x), _stream(stream)), "la_qkv_proj")
+    return q, k, v
+
+
+def attn_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, workspace=None, stream=None):
+    """softmax(scale q k^T) v: q [B,H,S_q,D], k/v [B,H,S_kv,D] -> [B,H,S_q,D]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    if k.shape != (B, H, S_kv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B,H,S_kv,D] matching q")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if kv_len is not None:
+        _need(kv_len, "kv_len")
+        if kv_len.dtype != torch.int32 or kv_len.shape != (B,):
+            raise ValueError("kv_len must be int32 [B]")
+    o = torch.empty_like(q) if out is None else out
+    if workspace is None and D in (64, 128) and q.dtype in _DT:
+        workspace = _workspace(workspace_size(LA_OP_ATTN_FWD, B, H, S_q, S_kv, D, q.dtype), q.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S_q, S_kv, D, int(bool(causal)), scale,
+                              _ptr(kv_len), _dt(q), _ptr(workspace), nbytes, _stream(stream)), "la_attn_fwd")
+    return o
+
+
+class KVCache:
+    """Caller-owned growing key/value cache [B,H,S_max,D] for the chunked mode."""
+
+    def __init__(self, B, H, S_max, D, dtype, device="cuda"):
+        self.k = torch.empty(B, H, S_max, D, dtype=dtype, device=device)
+        self.v = torch.empty(B, H, S_max, D, dtype=dtype, device=device)
+        self.c = la_kv_cache(self.k.data_ptr(), self.v.data_ptr(), B, H, D, S_max, 0, _DT[dtype])
+
+    @property
+    def len(self):
+        return self.c.len
+
+    def reset(self):
+        self.c.len = 0
+
+
+def attn_chunked(q_chunk, k_chunk, v_chunk, cache: KVCache, causal=True, scale=None, out=None, workspace=None,
+                 stream=None):
+    """Append this window's k/v to the cache, then attend q_chunk to the cache."""
+    for t, n in ((q_chunk, "q_chunk"), (k_chunk, "k_chunk"), (v_chunk, "v_chunk")):
+        _need(t, n)
+    B, H, C, D = q_chunk.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = torch.empty_like(q_chunk) if out is None else out
+    if workspace is None:
+        workspace = _workspace(workspace_size(LA_OP_ATTN_CHUNKED, B, H, C, cache.c.S_max, D, q_chunk.dtype),
+                               q_chunk.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_attn_chunked(_ptr(q_chunk), _ptr(k_chunk), _ptr(v_chunk), ctypes.byref(cache.c), _ptr(o), C,
+                                  int(bool(causal)), scale, _ptr(workspace), nbytes, _stream(stream)),
+           "la_attn_chunked")
+    return o
+
+
+def layer_attn(x, Wqkv, bqkv, H, causal=False, kv_len=None, out=None, workspace=None, stream=None):
+    """Projection + per-head attention + head merge: x [B,S,d] -> [B,S,d]."""
+    _need(x, "x")
+    B, S, dm = x.shape
+    D = dm // H if H > 0 else 0
+    o = torch.empty_like(x) if out is None else out
+    if workspace is None:
+        workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN, B, H, S, S, D, x.dtype), x.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_layer_attn(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(o), B, S, dm, H, int(bool(causal)),
+                                _ptr(kv_len), _dt(x), _ptr(workspace), nbytes, _stream(stream)), "la_layer_attn")
+    return o
+
+
+def get_last_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().la_get_last_error(_stream(stream)))

@@ -1,0 +1,413 @@
+// la_api.cu -- the C ABI of liblayerattn.so (declared in include/layerattn.h).
+//
+// Host side only: argument validation (before anything touches a device),
+// TMA tensor-map encoding, the split-KV plan, workspace carving and the
+// launches.  The library allocates no device memory.  The one piece of device
+// state is the error word below, which kernels latch when a bounded wait runs
+// out.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "la_device.cuh"
+#include "la_internal.h"
+
+__device__ uint32_t la_device_error_word;
+
+namespace la {
+namespace {
+
+// ---------------------------------------------------------------------------
+// small utilities
+// ---------------------------------------------------------------------------
+int elem_bytes(la_dtype dt) { return dt == LA_F32 ? 4 : 2; }
+bool dtype_ok(int dt) { return dt == LA_F32 || dt == LA_BF16 || dt == LA_F16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+la_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+uint32_t* error_word() {
+  static std::mutex mu;
+  static uint32_t* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, la_device_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
+CUtensorMapDataType tma_type(la_dtype dt) {
+  return dt == LA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                      : (dt == LA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+// 4-D map over a [B, H, rows, D] view (strides in elements), 128-byte swizzle.
+la_status map_bhsd(CUtensorMap* m, const void* base, la_dtype dt, int B, int H, long long rows, int D,
+                   long long s_row, long long s_head, long long s_batch, int box_rows, int box_cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return LA_ERR_CUDA;
+  const long long e = elem_bytes(dt);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows > 0 ? rows : 1),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row * e), static_cast<cuuint64_t>(s_head * e),
+                           static_cast<cuuint64_t>(s_batch * e)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, tma_type(dt), 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LA_OK : LA_ERR_CUDA;
+}
+
+// 2-D map over a row-major [rows, cols] matrix.
+la_status map_2d(CUtensorMap* m, const void* base, la_dtype dt, long long rows, long long cols, int box_rows,
+                 int box_cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return LA_ERR_CUDA;
+  const long long e = elem_bytes(dt);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * e)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, tma_type(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LA_OK : LA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// split-KV plan
+// ---------------------------------------------------------------------------
+struct Plan {
+  int num_qblk = 0;
+  int n_tiles = 0;  // key tiles of the longest query tile
+  int splits = 1;
+  int tiles_per_split = 1;
+  size_t ws_bytes = 0;  // partials the plan needs
+};
+
+size_t split_bytes(int splits, int B, int H, int S_q, int D) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(splits) * B * H * S_q;
+  return round_up(rows * D * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
+// Split the key range only when the unsplit grid leaves the GPU short of
+// full waves; estimate makespan as waves x tiles per CTA (+2 tiles of fixed
+// cost per CTA) and take the smallest, within what the workspace holds.
+Plan make_plan(la_dtype dt, int B, int H, int S_q, int S_kv, int D, size_t ws_avail, int sms) {
+  Plan p;
+  AttnShape sh;
+  attn_shape(dt, D, &sh);
+  p.num_qblk = (S_q + sh.rows_per_cta - 1) / sh.rows_per_cta;
+  p.n_tiles = (S_kv + sh.block_n - 1) / sh.block_n;
+  if (p.n_tiles < 1) p.n_tiles = 1;
+  p.tiles_per_split = p.n_tiles;
+  const long long ctas = static_cast<long long>(p.num_qblk) * B * H;
+  double best = 0.0;
+  for (int s = 1; s <= 16; ++s) {
+    if (s > 1 && p.n_tiles / s < 4) break;
+    if (static_cast<long long>(s) * B * H > 65535LL * 65535LL) break;
+    const size_t need = split_bytes(s, B, H, S_q, D);
+    if (need > ws_avail) break;
+    const int per = (p.n_tiles + s - 1) / s;
+    const long long waves = (ctas * s + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (per + 2) + (s > 1 ? 1.0 : 0.0);
+    if (s == 1 || cost < best * 0.95) {
+      best = cost;
+      p.splits = s;
+      p.tiles_per_split = per;
+      p.ws_bytes = need;
+    }
+  }
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// validation shared by the attention entry points
+// ---------------------------------------------------------------------------
+la_status check_attn_args(int B, int H, int S_q, int S_kv, int D, float scale, int dt) {
+  if (B < 1 || H < 1 || S_q < 0 || S_kv < 0) return LA_ERR_INVALID;
+  if (!dtype_ok(dt)) return LA_ERR_INVALID;
+  if (!(scale > 0.f) || !isfinite(scale)) return LA_ERR_INVALID;
+  if (D != 64 && D != 128) return LA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return LA_ERR_UNSUPPORTED;  // grid.y
+  return LA_OK;
+}
+
+// Attention over views: q [B,H,S_q,D] contiguous; k/v rows [0, S_kv) of a
+// [B,H,kv_rows_alloc,D] buffer; o with the given element strides.
+la_status run_attention(const void* q, const void* k, const void* v, long long kv_rows_alloc, void* o,
+                        long long o_sb, long long o_sh, long long o_ss, int B, int H, int S_q, int S_kv, int D,
+                        int causal, float scale, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes,
+                        cudaStream_t st) {
+  if (S_q == 0) return LA_OK;
+  AttnShape sh;
+  if (!attn_shape(dt, D, &sh)) return LA_ERR_UNSUPPORTED;
+  const Plan p = make_plan(dt, B, H, S_q, S_kv, D, ws == nullptr ? 0 : ws_bytes, device_sms());
+  uint32_t* err = error_word();
+  if (err == nullptr) return LA_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  la_status s;
+  s = map_bhsd(&tq, q, dt, B, H, S_q, D, D, static_cast<long long>(S_q) * D, static_cast<long long>(H) * S_q * D,
+               sh.box_q_rows, sh.box_cols);
+  if (s != LA_OK) return s;
+  s = map_bhsd(&tk, k, dt, B, H, S_kv, D, D, kv_rows_alloc * D, static_cast<long long>(H) * kv_rows_alloc * D,
+               sh.box_kv_rows, sh.box_cols);
+  if (s != LA_OK) return s;
+  s = map_bhsd(&tv, v, dt, B, H, S_kv, D, D, kv_rows_alloc * D, static_cast<long long>(H) * kv_rows_alloc * D,
+               sh.box_kv_rows, sh.box_cols);
+  if (s != LA_OK) return s;
+
+  AttnArgs a;
+  memset(&a, 0, sizeof a);
+  a.o = o;
+  a.o_sb = o_sb;
+  a.o_sh = o_sh;
+  a.o_ss = o_ss;
+  a.kv_len = kv_len;
+  a.B = B;
+  a.H = H;
+  a.S_q = S_q;
+  a.S_kv = S_kv;
+  a.causal = causal ? 1 : 0;
+  a.sl2 = scale * 1.4426950408889634f;
+  a.num_qblk = p.num_qblk;
+  a.tiles_per_split = p.tiles_per_split;
+  a.err = err;
+  if (p.splits > 1) {
+    const size_t rows = static_cast<size_t>(p.splits) * B * H * S_q;
+    a.part_o = static_cast<float*>(ws);
+    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round_up(rows * D * sizeof(float), 256));
+  }
+  cudaError_t e = launch_attn(dt, D, tq, tk, tv, a, p.splits, st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  if (p.splits > 1) {
+    CombineArgs c;
+    c.part_o = a.part_o;
+    c.part_lse = a.part_lse;
+    c.o = o;
+    c.o_sb = o_sb;
+    c.o_sh = o_sh;
+    c.o_ss = o_ss;
+    c.B = B;
+    c.H = H;
+    c.S_q = S_q;
+    c.D = D;
+    c.splits = p.splits;
+    e = launch_combine(dt, c, st);
+    if (e != cudaSuccess) return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+la_status check_proj_args(const void* x, const void* W, const void* bias, const void* q, const void* k,
+                          const void* v, int B, int S, int d_model, int H, float q_scale, int dt) {
+  if (!x || !W || !q || !k || !v) return LA_ERR_INVALID;
+  if (B < 1 || S < 0 || d_model < 1 || H < 1) return LA_ERR_INVALID;
+  if (!dtype_ok(dt) || !isfinite(q_scale)) return LA_ERR_INVALID;
+  if (d_model % H != 0) return LA_ERR_INVALID;
+  const int D = d_model / H;
+  if (D != 64 && D != 128) return LA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(W) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return LA_ERR_INVALID;
+  if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 3u)) return LA_ERR_INVALID;
+  if (static_cast<long long>(B) * S > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+  return LA_OK;
+}
+
+la_status run_proj(const void* x, const void* W, const void* bias, void* q, void* k, void* v, int B, int S,
+                   int d_model, int H, float q_scale, la_dtype dt, cudaStream_t st) {
+  const long long M = static_cast<long long>(B) * S;
+  if (M == 0) return LA_OK;
+  ProjShape ps;
+  if (!proj_shape(dt, &ps)) return LA_ERR_UNSUPPORTED;
+  uint32_t* err = error_word();
+  if (err == nullptr) return LA_ERR_CUDA;
+  CUtensorMap tx, tw;
+  la_status s = map_2d(&tx, x, dt, M, d_model, kTileM, ps.box_cols);
+  if (s != LA_OK) return s;
+  s = map_2d(&tw, W, dt, d_model, 3LL * d_model, ps.box_k_rows, ps.box_cols);
+  if (s != LA_OK) return s;
+  ProjArgs a;
+  a.bias = bias;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.M = static_cast<int>(M);
+  a.N = 3 * d_model;
+  a.K = d_model;
+  a.S = S;
+  a.H = H;
+  a.D = d_model / H;
+  a.q_scale = q_scale;
+  a.err = err;
+  return cuda_status(launch_proj(dt, tx, tw, a, st));
+}
+
+size_t layer_qkv_bytes(int B, int S, int d_model, la_dtype dt) {
+  return round_up(static_cast<size_t>(B) * S * d_model * elem_bytes(dt), 256);
+}
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+la_status la_qkv_proj(const void* x, const void* Wqkv, const void* bqkv, void* q, void* k, void* v, int B, int S,
+                      int d_model, int H, float q_scale, la_dtype dt, la_stream_t st) {
+  la_status s = check_proj_args(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt);
+  if (s != LA_OK) return s;
+  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, reinterpret_cast<cudaStream_t>(st));
+}
+
+la_status la_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int S_q, int S_kv,
+                      int D, int causal, float scale, const int32_t* kv_len, la_dtype dt, void* ws,
+                      size_t ws_bytes, la_stream_t st) {
+  // a pointer may be NULL only when its tensor is empty
+  if ((!q || !o) && S_q != 0) return LA_ERR_INVALID;
+  if ((!k || !v) && S_kv != 0) return LA_ERR_INVALID;
+  la_status s = check_attn_args(B, H, S_q, S_kv, D, scale, dt);
+  if (s != LA_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LA_ERR_INVALID;
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return LA_ERR_INVALID;
+  if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
+  if (S_q == 0) return LA_OK;
+  if (S_kv == 0) k = v = q;  // no key is ever loaded; the maps only need a valid base
+  return run_attention(q, k, v, S_kv, o, static_cast<long long>(H) * S_q * D, static_cast<long long>(S_q) * D, D,
+                       B, H, S_q, S_kv, D, causal, scale, kv_len, dt, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(st));
+}
+
+la_status la_attn_chunked(const void* q_chunk, const void* k_chunk, const void* v_chunk, la_kv_cache* cache,
+                          void* o_chunk, int chunk, int causal, float scale, void* ws, size_t ws_bytes,
+                          la_stream_t st) {
+  if (!cache || !q_chunk || !k_chunk || !v_chunk || !o_chunk || !cache->k || !cache->v) return LA_ERR_INVALID;
+  const int B = cache->B, H = cache->H, D = cache->D;
+  if (chunk < 0 || cache->len < 0 || cache->S_max < 1) return LA_ERR_INVALID;
+  if (static_cast<long long>(cache->len) + chunk > cache->S_max) return LA_ERR_INVALID;
+  la_status s = check_attn_args(B, H, chunk, cache->len + chunk, D, scale, cache->dtype);
+  if (s != LA_OK) return s;
+  if (!aligned16(q_chunk) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(o_chunk) ||
+      !aligned16(cache->k) || !aligned16(cache->v))
+    return LA_ERR_INVALID;
+  if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
+  if (chunk == 0) return LA_OK;
+  const la_dtype dt = cache->dtype;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
+  if (launch_kv_append(k_chunk, v_chunk, cache->k, cache->v, B, H, chunk, D, cache->S_max, cache->len,
+                       elem_bytes(dt), cs) != cudaSuccess)
+    return LA_ERR_CUDA;
+  const int S_kv = cache->len + chunk;
+  s = run_attention(q_chunk, cache->k, cache->v, cache->S_max, o_chunk, static_cast<long long>(H) * chunk * D,
+                    static_cast<long long>(chunk) * D, D, B, H, chunk, S_kv, D, causal, scale, nullptr, dt, ws,
+                    ws_bytes, cs);
+  if (s == LA_OK) cache->len = S_kv;
+  return s;
+}
+
+la_status la_layer_attn(const void* x, const void* Wqkv, const void* bqkv, void* o, int B, int S, int d_model,
+                        int H, int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes,
+                        la_stream_t st) {
+  if (!o || !ws) return LA_ERR_INVALID;
+  if (!aligned16(o) || !aligned16(ws)) return LA_ERR_INVALID;
+  // validate with placeholders for the q/k/v pointers, which live in ws
+  la_status s = check_proj_args(x, Wqkv, bqkv, ws, ws, ws, B, S, d_model, H, 1.f, dt);
+  if (s != LA_OK) return s;
+  const int D = d_model / H;
+  s = check_attn_args(B, H, S, S, D, 1.f, dt);
+  if (s != LA_OK) return s;
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return LA_ERR_INVALID;
+  const size_t one = layer_qkv_bytes(B, S, d_model, dt);
+  if (ws_bytes < 3 * one) return LA_ERR_WORKSPACE;
+  if (S == 0) return LA_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void *q = w, *k = w + one, *v = w + 2 * one;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
+  s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, cs);
+  if (s != LA_OK) return s;
+  const float scale = 1.0f / sqrtf(static_cast<float>(D));
+  return run_attention(q, k, v, S, o, static_cast<long long>(S) * d_model, D, d_model, B, H, S, S, D, causal,
+                       scale, kv_len, dt, w + 3 * one, ws_bytes - 3 * one, cs);
+}
+
+size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt) {
+  const size_t bad = static_cast<size_t>(-1);
+  if (check_attn_args(B, H, S_q, S_kv, D, 1.f, dt) != LA_OK) return bad;
+  const int sms = device_sms();
+  switch (op) {
+    case LA_OP_ATTN_FWD:
+    case LA_OP_ATTN_CHUNKED:
+      if (S_q == 0) return 0;
+      return make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), sms).ws_bytes;
+    case LA_OP_LAYER_ATTN: {
+      if (S_q != S_kv) return bad;
+      const size_t qkv = 3 * layer_qkv_bytes(B, S_q, H * D, dt);
+      if (S_q == 0) return qkv;
+      return qkv + make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), sms).ws_bytes;
+    }
+    default:
+      return bad;
+  }
+}
+
+la_status la_get_last_error(la_stream_t st) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(st));
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, la_device_error_word, sizeof w) != cudaSuccess) return LA_ERR_CUDA;
+  if (w != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(la_device_error_word, &zero, sizeof zero) != cudaSuccess) return LA_ERR_CUDA;
+  }
+  if (w & DEVERR_TIMEOUT) return LA_ERR_TIMEOUT;
+  if (w & DEVERR_INTERNAL) return LA_ERR_INTERNAL;
+  return LA_OK;
+}
+
+const char* la_status_string(la_status s) {
+  switch (s) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_INVALID: return "LA_ERR_INVALID: invalid argument";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: unsupported head dim, dtype or size";
+    case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace too small";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime call or launch failed";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a device-side wait ran out";
+    case LA_ERR_INTERNAL: return "LA_ERR_INTERNAL: device consistency check failed";
+  }
+  return "unknown la_status";
+}
+
+}  // extern "C"

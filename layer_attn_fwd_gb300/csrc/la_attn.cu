@@ -1,0 +1,532 @@
+// la_attn.cu -- attention forward on sm_103a: O = softmax(scale Q K^T) V.
+//
+// The method is online softmax over key/value tiles ("GPU Kernel for a
+// Transformer Layer", section What we learned: a running row max, row sum and
+// output accumulator carried across key/value blocks, so the
+// [B, H, S_q, S_kv] score matrix is never formed), applied to the attention
+// equation of "Shape-Aware Attention" (section Inspiration), with causal and
+// key-padding masks.
+//
+// One CTA owns NQ query tiles of 128 rows of one (batch, head) and walks a
+// range of 128-key tiles (the whole causal/padded range, or one split of it):
+//
+//   warp 4*NQ   (TMA)      loads Q once, then K_j / V_j through an NS-stage
+//                          ring of shared-memory buffers (128-byte swizzle).
+//   warp 4*NQ+1 (MMA)      one thread issues tcgen05.mma:  S_t = Q_t K_j^T into
+//                          tensor memory, then O_t += P_t V_j with P_t read
+//                          straight from tensor memory (A operand in TMEM).
+//   warps 4t..4t+3         softmax of query tile t: thread r owns row r of
+//   (softmax, tile t)      S_t (tcgen05.ld 32x32b), applies the mask, keeps
+//                          the running max m and sum l in registers, writes
+//                          P = exp2(S*scale*log2e - m) back over S (bf16/f16
+//                          packed pairs, or tf32), and rescales O_t in tensor
+//                          memory when the max grows; finally O_t / l -> HBM.
+//
+// The two query tiles ping-pong: while tile 0's softmax runs, the tensor core
+// computes PV and the next QK^T of tile 1, and vice versa.  Per tile the MMA
+// thread issues PV_t(j) before S_t(j+1), so when the softmax sees S_t(j+1)
+// complete, PV_t(j) is complete as well; the O rescale and the P overwrite
+// need no other wait.
+//
+// The max is only moved (and O rescaled) when it grows by more than 2^8; P is
+// then bounded by 256 and the final O / l stays exact because both use the
+// same stale max.
+//
+// Every wait is bounded (la_device.cuh); a wait that runs out latches the
+// device error word and the CTA winds down, freeing its tensor memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "la_device.cuh"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr uint32_t ab = AB_BF16;
+  static constexpr bool tf32 = false;
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+template <>
+struct Elem<__half> {
+  static constexpr uint32_t ab = AB_F16;
+  static constexpr bool tf32 = false;
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+template <>
+struct Elem<float> {
+  static constexpr uint32_t ab = AB_TF32;
+  static constexpr bool tf32 = true;
+};
+
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p *= 2;
+  return p;
+}
+
+template <typename T, int D_, int NQ_, int BN_, int NS_>
+struct Cfg {
+  static constexpr int D = D_, NQ = NQ_, BN = BN_, NS = NS_;
+  static constexpr int E = sizeof(T);
+  static constexpr int CW = 128 / E;            // elements per 128-byte swizzle row
+  static constexpr int NCH = D / CW;            // 128-byte chunks per row of D elements
+  static constexpr int Q_CHUNK = kTileM * 128;  // bytes of one chunk of a Q tile
+  static constexpr int KV_CHUNK = BN * 128;
+  static constexpr int Q_TILE = NCH * Q_CHUNK;
+  static constexpr int KV_TILE = NCH * KV_CHUNK;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
+  static constexpr int OFF_V = OFF_K + NS * KV_TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * KV_TILE;
+  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ], mma_done
+  static constexpr int NBAR = 1 + 4 * NS + 3 * NQ + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int TILE_COLS = BN + D;                 // TMEM columns per query tile: S|P, then O
+  static constexpr int TMEM_COLS = pow2_at_least(NQ * TILE_COLS);
+  static constexpr int QK_STEPS = D * E / 32;              // one MMA consumes 32 bytes of a row
+  static constexpr int PV_ROWS = 32 / E;                   // keys per PV MMA (16, or 8 for tf32)
+  static constexpr int PV_STEPS = BN / PV_ROWS;
+  static constexpr int THREADS = NQ * 128 + 64;
+  static constexpr int WARP_TMA = NQ * 4;
+  static constexpr int WARP_MMA = NQ * 4 + 1;
+  static_assert(D % CW == 0, "head dim must fill whole 128-byte rows");
+  static_assert(TMEM_COLS <= 512, "tensor memory budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(BN == 64 || BN == 128, "key tile");
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// TMEM -> registers for a full row of BN fp32 scores.
+template <int BN>
+__device__ __forceinline__ void load_row(uint32_t taddr, uint32_t (&s)[BN]) {
+  if constexpr (BN == 128) {
+    tmem_ld_x128(taddr, s);
+  } else {
+    tmem_ld_x64(taddr, s);
+  }
+}
+
+// Store P (already exponentiated, in s[] as fp32 bits) over the S columns.
+template <typename T, int BN>
+__device__ __forceinline__ void store_p(uint32_t taddr, uint32_t (&s)[BN]) {
+  if constexpr (Elem<T>::tf32) {
+#pragma unroll
+    for (int h = 0; h < BN / 64; ++h) {
+      uint32_t a[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) a[c] = f32_to_tf32(u2f(s[64 * h + c]));
+      tmem_st_x64(taddr + 64 * h, a);
+    }
+  } else {
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int c = 0; c < BN / 2; ++c) pk[c] = Elem<T>::pack2(u2f(s[2 * c]), u2f(s[2 * c + 1]));
+    if constexpr (BN == 128) {
+      tmem_st_x64(taddr, pk);
+    } else {
+      tmem_st_x32(taddr, pk);
+    }
+  }
+}
+
+// 32 fp32 values -> 32 output elements at dst (16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void store_out32(T* dst, const float (&v)[32]) {
+  if constexpr (Elem<T>::tf32) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 w;
+      w.x = Elem<T>::pack2(v[8 * i + 0], v[8 * i + 1]);
+      w.y = Elem<T>::pack2(v[8 * i + 2], v[8 * i + 3]);
+      w.z = Elem<T>::pack2(v[8 * i + 4], v[8 * i + 5]);
+      w.w = Elem<T>::pack2(v[8 * i + 6], v[8 * i + 7]);
+      d4[i] = w;
+    }
+  }
+}
+
+template <typename T, int D, int NQ, int BN, int NS>
+__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+  using C = Cfg<T, D, NQ, BN, NS>;
+  constexpr bool TF32 = Elem<T>::tf32;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + NS;
+  uint64_t* v_full = k_empty + NS;
+  uint64_t* v_empty = v_full + NS;
+  uint64_t* s_full = v_empty + NS;
+  uint64_t* p_full = s_full + NQ;
+  uint64_t* o_full = p_full + NQ;
+  uint64_t* mma_done = o_full + NQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which work this CTA owns ------------------------------------------
+  // Causal: the heaviest query blocks (last rows) go first.
+  const int qblk = a.causal ? (a.num_qblk - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int b = bh / a.H;
+  const int h = bh - b * a.H;
+  const int split = blockIdx.z;
+  const int off = a.S_kv - a.S_q;  // query row i is absolute position i + off
+  int kv_lim = a.S_kv;
+  if (a.kv_len != nullptr) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
+  const int jb = split * a.tiles_per_split;  // first key tile of this split
+  int je[NQ];                                // one past the last key tile, per query tile
+  int je_all = jb;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int q_lo = (qblk * NQ + t) * kTileM;
+    int n = 0;
+    if (q_lo < a.S_q) {
+      int hi = kv_lim;
+      if (a.causal) hi = min(hi, min(q_lo + kTileM - 1, a.S_q - 1) + off + 1);
+      n = hi > 0 ? (hi + BN - 1) / BN : 0;
+    }
+    je[t] = max(jb, min(n, jb + a.tiles_per_split));
+    je_all = max(je_all, je[t]);
+  }
+
+  // ---- set-up ---------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);  // one arrive per softmax warp
+      mbar_init(&o_full[t], 1);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{a.err, abort_flag};
+
+  if (warp == C::WARP_TMA) {
+    // ======================= TMA producer ==================================
+    int last_k[NS], last_v[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
+    bool q_issued = false;
+    if (lane == 0 && je_all > jb) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
+      for (int t = 0; t < NQ; ++t)
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
+                      (qblk * NQ + t) * kTileM, h, b, pol_q);
+      q_issued = true;
+      for (int j = jb; j < je_all; ++j) {
+        const int i = j - jb, s = i % NS, r = i / NS;
+        if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab)) break;
+        mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(&tm_k, &k_full[s], smem + C::OFF_K + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
+                      j * BN, h, b, pol_kv);
+        last_k[s] = r;
+        if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab)) break;
+        mbar_arrive_expect_tx(&v_full[s], C::KV_TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(&tm_v, &v_full[s], smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
+                      j * BN, h, b, pol_kv);
+        last_v[s] = r;
+      }
+    }
+    __syncwarp();
+    __syncthreads();  // teardown rendezvous
+    if (lane == 0 && *abort_flag) {
+      // let the copies still in flight land before the CTA's shared memory goes away
+      if (q_issued) mbar_wait_teardown(q_full, 0);
+      for (int s = 0; s < NS; ++s) {
+        if (last_k[s] >= 0) mbar_wait_teardown(&k_full[s], last_k[s] & 1);
+        if (last_v[s] >= 0) mbar_wait_teardown(&v_full[s], last_v[s] & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == C::WARP_MMA) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0 && je_all > jb) {
+      const uint32_t idesc_qk = idesc_make(Elem<T>::ab, kTileM, BN, false, false);
+      const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      // S_t = Q_t K_j^T: both operands K-major; one MMA per 32 bytes of a row.
+      auto issue_s = [&](int t, int j) {
+        const int s = (j - jb) % NS;
+        const uint32_t d = tmem + t * C::TILE_COLS;
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+          const uint32_t o = (kk & 3) * 32;  // byte offset inside the 128-byte row
+          const uint64_t ad = sdesc_sw128(sQ + t * C::Q_TILE + (kk >> 2) * C::Q_CHUNK + o, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + s * C::KV_TILE + (kk >> 2) * C::KV_CHUNK + o, 16, 1024);
+          mma_ss<TF32>(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V_j: P from tensor memory, V MN-major (rows = keys).
+      auto issue_pv = [&](int t, int j) {
+        const int s = (j - jb) % NS;
+        const uint32_t d = tmem + t * C::TILE_COLS + BN;
+        const uint32_t p = tmem + t * C::TILE_COLS;
+#pragma unroll
+        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+          const uint64_t bd = sdesc_sw128(sV + s * C::KV_TILE + kk * C::PV_ROWS * 128, C::KV_CHUNK, 1024);
+          mma_ts<TF32>(d, p + kk * 8, bd, idesc_pv, (j > jb || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, ab) && mbar_wait(&k_full[0], 0, ab);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < NQ; ++t) {
+          if (je[t] > jb) {
+            issue_s(t, jb);
+            mma_commit(&s_full[t]);
+          }
+        }
+        mma_commit(&k_empty[0]);
+      }
+      for (int j = jb; ok && j < je_all; ++j) {
+        const int i = j - jb, s = i % NS, r = i / NS;
+        const int sn = (i + 1) % NS, rn = (i + 1) / NS;
+        bool v_ready = false, k_next = false;
+        for (int t = 0; t < NQ && ok; ++t) {
+          if (j >= je[t]) continue;
+          if (!mbar_wait(&p_full[t], i & 1, ab)) { ok = false; break; }
+          if (!v_ready) {
+            if (!mbar_wait(&v_full[s], r & 1, ab)) { ok = false; break; }
+            v_ready = true;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < je[t]) {
+            if (!k_next) {
+              if (!mbar_wait(&k_full[sn], rn & 1, ab)) { ok = false; break; }
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, j + 1);
+            mma_commit(&s_full[t]);
+          } else {
+            mma_commit(&o_full[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&v_empty[s]);
+        if (k_next) mma_commit(&k_empty[sn]);
+      }
+    }
+    __syncwarp();
+    __syncthreads();  // teardown rendezvous
+    if (*abort_flag) {
+      if (lane == 0) {
+        mma_commit(mma_done);  // fires once every MMA issued so far has finished
+        mbar_wait_teardown(mma_done, 0);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  } else {
+    // ======================= softmax of query tile t ========================
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int q_lo = (qblk * NQ + t) * kTileM;
+    const int q_row = q_lo + row;
+    const int r_abs = q_row + off;
+    const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * C::TILE_COLS;
+    const uint32_t tO = tS + BN;
+    const float sl2 = a.sl2;
+    float m_run = -INFINITY;  // running max, in log2 units of the scaled scores
+    float l = 0.f;            // running sum of P
+    bool ok = true;
+    for (int j = jb; j < je[t]; ++j) {
+      const int i = j - jb;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], i & 1, ab));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[BN];
+      load_row<BN>(tS, s);
+      const int kv0 = j * BN;
+      if (kv0 + BN > kv_lim || (a.causal && kv0 + BN - 1 > q_lo + off)) {
+        int lim = kv_lim;
+        if (a.causal) lim = min(lim, r_abs + 1);
+        lim -= kv0;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= lim) s[c] = f2u(-INFINITY);
+      }
+      float mx = u2f(s[0]);
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, u2f(s[c]));
+      const float m_new = fmaxf(m_run, mx * sl2);
+      const bool grow = m_new > m_run + 8.0f;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2_approx(m_run - m_new);  // 0 on the first visible key
+        l *= alpha;
+        m_run = m_new;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const float p = ex2_approx(fmaf(u2f(s[c]), sl2, -m_use));
+        rs += p;
+        s[c] = f2u(p);
+      }
+      l += rs;
+      store_p<T, BN>(tS, s);
+      if (grow && j > jb) {
+        // O was produced by PV of earlier tiles: rescale it to the new max.
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = f2u(u2f(o[c]) * alpha);
+          tmem_st_x32(tO + c0, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
+    }
+    const bool has_o = je[t] > jb;
+    if (ok && has_o) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, ab));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool row_ok = q_row < a.S_q;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (a.part_o != nullptr) {
+        const size_t prow = (static_cast<size_t>(split) * a.B * a.H + bh) * a.S_q + q_row;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (has_o) tmem_ld_x32(tO + c0, o);
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = has_o ? u2f(o[c]) * inv : 0.f;
+          if (row_ok) store_out32<float>(a.part_o + prow * D + c0, v);
+        }
+        if (row_ok) a.part_lse[prow] = l > 0.f ? m_run + __log2f(l) : -INFINITY;
+      } else {
+        T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + static_cast<long long>(q_row) * a.o_ss;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (has_o) tmem_ld_x32(tO + c0, o);
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = has_o ? u2f(o[c]) * inv : 0.f;
+          if (row_ok) store_out32<T>(dst + c0, v);
+        }
+      }
+    }
+    __syncthreads();  // teardown rendezvous
+  }
+}
+
+template <typename T, int D, int NQ, int BN, int NS>
+cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                       int splits, cudaStream_t st) {
+  using C = Cfg<T, D, NQ, BN, NS>;
+  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  dim3 grid(a.num_qblk, a.B * a.H, splits);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Launch shapes per (dtype, D): query rows per CTA = 128 * NQ, key tile BN,
+// stages NS; chosen so Q + NS stages of K and V fit in 227 KB of shared memory
+// and the S|P and O columns of the NQ tiles fit in 512 TMEM columns.
+bool attn_shape(la_dtype dt, int D, AttnShape* s) {
+  const int e = dt == LA_F32 ? 4 : 2;
+  if (D != 64 && D != 128) return false;
+  if (dt != LA_F32 && dt != LA_BF16 && dt != LA_F16) return false;
+  const bool single = (dt == LA_F32 && D == 128);
+  s->rows_per_cta = single ? 128 : 256;
+  s->block_n = single ? 64 : 128;
+  s->box_q_rows = kTileM;
+  s->box_kv_rows = s->block_n;
+  s->box_cols = 128 / e;
+  return true;
+}
+
+cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const AttnArgs& a, int splits, cudaStream_t st) {
+  switch (dt) {
+    case LA_BF16:
+      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3>(tq, tk, tv, a, splits, st)
+                     : launch_one<__nv_bfloat16, 128, 2, 128, 2>(tq, tk, tv, a, splits, st);
+    case LA_F16:
+      return D == 64 ? launch_one<__half, 64, 2, 128, 3>(tq, tk, tv, a, splits, st)
+                     : launch_one<__half, 128, 2, 128, 2>(tq, tk, tv, a, splits, st);
+    case LA_F32:
+      return D == 64 ? launch_one<float, 64, 2, 128, 2>(tq, tk, tv, a, splits, st)
+                     : launch_one<float, 128, 1, 64, 2>(tq, tk, tv, a, splits, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

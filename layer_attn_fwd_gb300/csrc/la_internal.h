@@ -1,0 +1,79 @@
+// la_internal.h -- contract between the C-ABI layer (la_api.cu) and the kernel
+// translation units.  Host code only passes plain structs and CUtensorMaps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layerattn.h"
+
+namespace la {
+
+// Rows of one query tile (the M of every tcgen05 MMA here).
+constexpr int kTileM = 128;
+
+// Arguments of the attention kernel (everything but the tensor maps).
+struct AttnArgs {
+  void* o;                    // output base (unsplit launch)
+  long long o_sb, o_sh, o_ss; // output strides in elements: batch, head, row
+  float* part_o;              // split partials [splits][B*H][S_q][D] (split launch) or null
+  float* part_lse;            // split log2-sum-exp [splits][B*H][S_q] or null
+  const int32_t* kv_len;      // [B] or null
+  int B, H, S_q, S_kv;
+  int causal;
+  float sl2;                  // softmax scale times log2(e)
+  int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
+  int tiles_per_split;        // key tiles handled by one split
+  uint32_t* err;              // device error word
+};
+
+// Static launch shape of the attention kernel for a dtype and head dim.
+struct AttnShape {
+  int rows_per_cta;   // query rows per CTA
+  int block_n;        // keys per tile
+  int box_q_rows;     // TMA box rows for q
+  int box_kv_rows;    // TMA box rows for k / v
+  int box_cols;       // TMA box columns (one 128-byte swizzle row)
+};
+bool attn_shape(la_dtype dt, int D, AttnShape* s);
+
+// Launch the attention kernel over grid (num_qblk, B*H, splits).
+cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const AttnArgs& a, int splits, cudaStream_t st);
+
+// Merge split partials into o.
+struct CombineArgs {
+  const float* part_o;
+  const float* part_lse;
+  void* o;
+  long long o_sb, o_sh, o_ss;
+  int B, H, S_q, D, splits;
+};
+cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st);
+
+// Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`.
+cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
+                             int rows, int D, int S_max, int at, int elem_bytes, cudaStream_t st);
+
+// Fused Q/K/V projection.
+struct ProjArgs {
+  const void* bias;
+  void* q;
+  void* k;
+  void* v;
+  int M, N, K;        // rows (B*S), 3*d_model, d_model
+  int S, H, D;
+  float q_scale;
+  uint32_t* err;
+};
+struct ProjShape {
+  int block_n;        // output columns per CTA
+  int box_cols;       // TMA box columns (one 128-byte swizzle row)
+  int box_k_rows;     // TMA box rows of the weight tile (= K per stage)
+};
+bool proj_shape(la_dtype dt, ProjShape* s);
+cudaError_t launch_proj(la_dtype dt, const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a,
+                        cudaStream_t st);
+
+}  // namespace la

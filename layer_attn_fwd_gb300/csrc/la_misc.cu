@@ -1,0 +1,128 @@
+// la_misc.cu -- the memory-bound helpers of the path:
+//   - split-KV merge: partial outputs O_s (each normalised by its own sum)
+//     and their log2-sum-exp values lse_s combine as
+//       o = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M),  M = max_s lse_s,
+//     the same rescaling algebra the online softmax applies tile by tile;
+//   - key/value cache append for the chunked long-context mode ("Roofline",
+//     section How we built it: windows against a growing key/value cache).
+// Both are plain coalesced 16-byte streams with grids sized to the SM count.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "la_device.cuh"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+__device__ __forceinline__ void store4(float* d, float a, float b, float c, float e) {
+  *reinterpret_cast<float4*>(d) = make_float4(a, b, c, e);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* d, float a, float b, float c, float e) {
+  __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, e);
+  uint2 w;
+  w.x = *reinterpret_cast<uint32_t*>(&x);
+  w.y = *reinterpret_cast<uint32_t*>(&y);
+  *reinterpret_cast<uint2*>(d) = w;
+}
+__device__ __forceinline__ void store4(__half* d, float a, float b, float c, float e) {
+  __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, e);
+  uint2 w;
+  w.x = *reinterpret_cast<uint32_t*>(&x);
+  w.y = *reinterpret_cast<uint32_t*>(&y);
+  *reinterpret_cast<uint2*>(d) = w;
+}
+
+// One thread per (row, 4 consecutive columns).
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  const int vec = a.D / 4;
+  const long long rows = static_cast<long long>(a.B) * a.H * a.S_q;
+  const long long total = rows * vec;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = g / vec;
+    const int c = static_cast<int>(g - row * vec) * 4;
+    float M = -INFINITY;
+    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.part_lse[s * rows + row]);
+    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f, wsum = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < a.splits; ++s) {
+        const float w = ex2_approx(a.part_lse[s * rows + row] - M);
+        const float4 o = *reinterpret_cast<const float4*>(a.part_o + (s * rows + row) * a.D + c);
+        wsum += w;
+        x0 = fmaf(w, o.x, x0);
+        x1 = fmaf(w, o.y, x1);
+        x2 = fmaf(w, o.z, x2);
+        x3 = fmaf(w, o.w, x3);
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const long long bh = row / a.S_q;
+    const long long i = row - bh * a.S_q;
+    const long long b = bh / a.H, h = bh - b * a.H;
+    T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + i * a.o_ss + c;
+    store4(dst, x0 * inv, x1 * inv, x2 * inv, x3 * inv);
+  }
+}
+
+// blockIdx.y selects k (0) or v (1).
+__global__ void __launch_bounds__(256)
+    kv_append_kernel(const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint8_t* k_dst,
+                     uint8_t* v_dst, long long n_vec, int vec_per_row, int rows, long long dst_head_bytes,
+                     long long at_bytes) {
+  const uint4* src = blockIdx.y == 0 ? k_src : v_src;
+  uint8_t* dst = blockIdx.y == 0 ? k_dst : v_dst;
+  const long long row_bytes = static_cast<long long>(vec_per_row) * 16;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < n_vec;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = g / vec_per_row;  // row over all (b, h)
+    const long long c = g - r * vec_per_row;
+    const long long bh = r / rows;
+    const long long rr = r - bh * rows;
+    *reinterpret_cast<uint4*>(dst + bh * dst_head_bytes + at_bytes + rr * row_bytes + c * 16) = src[g];
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
+  const long long total = static_cast<long long>(a.B) * a.H * a.S_q * (a.D / 4);
+  if (total == 0) return cudaSuccess;
+  const long long want = (total + 255) / 256;
+  const int cap = sm_count() * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  switch (dt) {
+    case LA_F32: combine_kernel<float><<<grid, 256, 0, st>>>(a); break;
+    case LA_BF16: combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a); break;
+    case LA_F16: combine_kernel<__half><<<grid, 256, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
+                             int rows, int D, int S_max, int at, int elem_bytes, cudaStream_t st) {
+  const int vec_per_row = D * elem_bytes / 16;
+  const long long n_vec = static_cast<long long>(B) * H * rows * vec_per_row;
+  if (n_vec == 0) return cudaSuccess;
+  const long long want = (n_vec + 255) / 256;
+  const int cap = sm_count() * 4;
+  dim3 grid(static_cast<unsigned>(want < cap ? want : cap), 2);
+  const long long row_bytes = static_cast<long long>(D) * elem_bytes;
+  kv_append_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(k_src),
+                                         reinterpret_cast<const uint4*>(v_src), reinterpret_cast<uint8_t*>(k_dst),
+                                         reinterpret_cast<uint8_t*>(v_dst), n_vec, vec_per_row, rows,
+                                         static_cast<long long>(S_max) * row_bytes,
+                                         static_cast<long long>(at) * row_bytes);
+  return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,113 @@
+"""The C ABI on a machine without a GPU: the library builds, loads, exports
+every entry point declared in include/layerattn.h, and rejects invalid calls
+on the host before touching any device.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from layer_attn_fwd_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "layerattn.h")
+
+# plausible, 256-byte aligned addresses that validation must reject before use
+FAKE = ctypes.c_void_p(0x7f0000000000)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_workspace_size",
+            "la_get_last_error", "la_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert api.status_string(s).startswith("LA_")
+    assert "unknown" in api.status_string(99)
+
+
+def _attn(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, S_q=16, S_kv=16, D=64, causal=0, scale=0.125,
+          kv_len=None, dt=api.LA_BF16, ws=None, ws_bytes=0):
+    return lib.la_attn_fwd(q, k, v, o, B, H, S_q, S_kv, D, causal, scale, kv_len, dt, ws, ws_bytes, None)
+
+
+def test_attn_fwd_rejects_bad_arguments(lib):
+    assert _attn(lib, q=None) == api.LA_ERR_INVALID
+    assert _attn(lib, o=None) == api.LA_ERR_INVALID
+    assert _attn(lib, B=0) == api.LA_ERR_INVALID
+    assert _attn(lib, H=-1) == api.LA_ERR_INVALID
+    assert _attn(lib, S_q=-1) == api.LA_ERR_INVALID
+    assert _attn(lib, S_kv=-5) == api.LA_ERR_INVALID
+    assert _attn(lib, scale=0.0) == api.LA_ERR_INVALID
+    assert _attn(lib, scale=-1.0) == api.LA_ERR_INVALID
+    assert _attn(lib, scale=float("inf")) == api.LA_ERR_INVALID
+    assert _attn(lib, scale=float("nan")) == api.LA_ERR_INVALID
+    assert _attn(lib, dt=7) == api.LA_ERR_INVALID
+    assert _attn(lib, q=ctypes.c_void_p(0x7f0000000008)) == api.LA_ERR_INVALID   # not 16-byte aligned
+    assert _attn(lib, kv_len=ctypes.c_void_p(0x7f0000000002)) == api.LA_ERR_INVALID
+    assert _attn(lib, D=96) == api.LA_ERR_UNSUPPORTED
+    assert _attn(lib, D=32) == api.LA_ERR_UNSUPPORTED
+    assert _attn(lib, B=300, H=300) == api.LA_ERR_UNSUPPORTED                     # B*H > grid limit
+
+
+def test_qkv_proj_rejects_bad_arguments(lib):
+    def call(x=FAKE, W=FAKE, b=None, B=2, S=8, dm=128, H=2, qs=1.0, dt=api.LA_F32):
+        return lib.la_qkv_proj(x, W, b, FAKE, FAKE, FAKE, B, S, dm, H, qs, dt, None)
+    assert call(x=None) == api.LA_ERR_INVALID
+    assert call(dm=129, H=2) == api.LA_ERR_INVALID        # d_model not a multiple of H
+    assert call(dm=192, H=2) == api.LA_ERR_UNSUPPORTED    # D = 96
+    assert call(S=-1) == api.LA_ERR_INVALID
+    assert call(qs=float("nan")) == api.LA_ERR_INVALID
+    assert call(b=ctypes.c_void_p(0x7f0000000001)) == api.LA_ERR_INVALID
+
+
+def test_layer_attn_checks_workspace_before_launch(lib):
+    need = api.workspace_size(api.LA_OP_LAYER_ATTN, 8, 8, 512, 512, 64, api.torch.float32)
+    assert need >= 3 * 8 * 512 * 512 * 4
+    st = lib.la_layer_attn(FAKE, FAKE, None, FAKE, 8, 512, 512, 8, 0, None, api.LA_F32, FAKE, 3 * 8 * 512 * 512 * 4 - 1,
+                           None)
+    assert st == api.LA_ERR_WORKSPACE
+    st = lib.la_layer_attn(FAKE, FAKE, None, FAKE, 8, 512, 512, 8, 0, None, api.LA_F32, None, need, None)
+    assert st == api.LA_ERR_INVALID
+
+
+def test_chunked_rejects_overflowing_cache_and_keeps_len(lib):
+    c = api.la_kv_cache(0x7f0000000000, 0x7f0000100000, 2, 16, 64, 100, 90, api.LA_BF16)
+    st = lib.la_attn_chunked(FAKE, FAKE, FAKE, ctypes.byref(c), FAKE, 11, 1, 0.125, None, 0, None)
+    assert st == api.LA_ERR_INVALID
+    assert c.len == 90
+    c.D = 80
+    st = lib.la_attn_chunked(FAKE, FAKE, FAKE, ctypes.byref(c), FAKE, 5, 1, 0.125, None, 0, None)
+    assert st == api.LA_ERR_UNSUPPORTED
+    assert c.len == 90
+
+
+def test_workspace_sizes(lib):
+    bad = ctypes.c_size_t(-1).value
+    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 1, 1, 16, 16, 96, api.LA_BF16) == bad
+    assert lib.la_workspace_size(9, 1, 1, 16, 16, 64, api.LA_BF16) == bad
+    assert lib.la_workspace_size(api.LA_OP_LAYER_ATTN, 1, 1, 16, 32, 64, api.LA_BF16) == bad
+    # short key ranges never split
+    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_F32) == 0
+    # the 100k-token chunked case: partials stay far below the cache itself
+    n = lib.la_workspace_size(api.LA_OP_ATTN_CHUNKED, 2, 16, 4096, 100000, 64, api.LA_BF16)
+    assert n != bad and n < 2 * 16 * 100000 * 64 * 2 * 4
+    # one long row range on a small grid splits, and asks for room for it
+    n = lib.la_workspace_size(api.LA_OP_ATTN_FWD, 1, 1, 256, 8192, 128, api.LA_BF16)
+    assert n >= 2 * 256 * 128 * 4

@@ -1,0 +1,135 @@
+"""Attention forward on the GPU through the C ABI, element by element against
+the fp64 oracle on identical seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL, assert_close, need_gpu
+from layer_attn_fwd_gb300 import api, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [torch.float32, torch.bfloat16, torch.float16]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    need_gpu()
+    build.build()
+    api.load()
+
+
+def _gpu_attn(q, k, v, causal, kv_len=None, split=True, scale=None):
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    kl = kv_len.cuda() if kv_len is not None else None
+    ws = None if split else torch.empty(0, dtype=torch.uint8, device="cuda")
+    o = api.attn_fwd(qd, kd, vd, causal=causal, scale=scale, kv_len=kl, workspace=ws)
+    assert api.get_last_error() == api.LA_OK
+    return o
+
+
+def test_c1_seed_sweep():
+    """fp32, non-causal, B=1 H=2 S=128 D=64 over 40 seeds."""
+    for seed in range(40):
+        q, k, v = inputs.attn_inputs(1, 2, 128, 128, 64, torch.float32, seed=seed)
+        o = _gpu_attn(q, k, v, False)
+        assert_close(o, oracle.attn(q, k, v), torch.float32, f"seed {seed}")
+
+
+SHAPES = [(2, 3, 300, 300), (1, 2, 77, 519), (1, 1, 519, 77), (2, 2, 1, 1), (1, 2, 1, 700), (3, 1, 256, 256)]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shapes(dtype, D, causal, shape):
+    B, H, S_q, S_kv = shape
+    q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, dtype, seed=S_q * 7 + S_kv + D)
+    o = _gpu_attn(q, k, v, causal)
+    assert_close(o, oracle.attn(q, k, v, causal=causal), dtype, f"{shape} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding(dtype, causal):
+    B, H, S, D = 5, 2, 333, 64
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, dtype, seed=11)
+    kv_len = torch.tensor([333, 250, 0, 1, 1000], dtype=torch.int32)  # 1000 clamps to S
+    o = _gpu_attn(q, k, v, causal, kv_len=kv_len)
+    want = oracle.attn(q, k, v, causal=causal, kv_len=kv_len)
+    assert_close(o, want, dtype, "padding")
+    assert torch.count_nonzero(o[2]).item() == 0  # no visible key -> zero rows
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float16, 64), (torch.float32, 64),
+                                     (torch.float32, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_kv_equals_unsplit(dtype, D, causal):
+    B, H, S_q, S_kv = 1, 2, 256, 4096 + 77
+    assert api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S_q, S_kv, D, dtype) > 0  # the plan splits
+    q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, dtype, seed=12)
+    o_split = _gpu_attn(q, k, v, causal, split=True)
+    o_one = _gpu_attn(q, k, v, causal, split=False)
+    want = oracle.attn(q, k, v, causal=causal)
+    assert_close(o_split, want, dtype, "split")
+    assert_close(o_one, want, dtype, "unsplit")
+    assert_close(o_split, o_one.double().cpu().numpy(), dtype, "split vs unsplit")
+
+
+def test_scale_parameter():
+    q, k, v = inputs.attn_inputs(2, 2, 200, 200, 64, torch.bfloat16, seed=13)
+    for scale in (0.01, 0.3):
+        o = _gpu_attn(q, k, v, True, scale=scale)
+        assert_close(o, oracle.attn(q, k, v, causal=True, scale=scale), torch.bfloat16, f"scale {scale}")
+
+
+def test_repeat_runs_bitwise_identical():
+    q, k, v = inputs.attn_inputs(2, 4, 1000, 1000, 128, torch.bfloat16, seed=14)
+    a = _gpu_attn(q, k, v, True)
+    b = _gpu_attn(q, k, v, True)
+    assert torch.equal(a, b)
+
+
+def test_empty_sizes():
+    q, k, v = inputs.attn_inputs(2, 2, 0, 50, 64, torch.bfloat16, seed=15)
+    o = _gpu_attn(q, k, v, False)
+    assert o.shape == (2, 2, 0, 64)
+    q, k, v = inputs.attn_inputs(2, 2, 40, 0, 64, torch.bfloat16, seed=16)
+    o = _gpu_attn(q, k, v, False)
+    assert torch.count_nonzero(o).item() == 0
+
+
+def test_large_scores_no_overflow():
+    q, k, v = inputs.attn_inputs(1, 2, 256, 256, 64, torch.float32, seed=17)
+    q = q * 300.0
+    o = _gpu_attn(q, k, v, False)
+    assert_close(o, oracle.attn(q, k, v), torch.float32, "large scores")
+
+
+def _sampled(o, rows):
+    r = rows.numpy()
+    return o[r[:, 0], r[:, 1], r[:, 2]]
+
+
+@pytest.mark.parametrize("padded", [False, True])
+def test_workload_fp32_causal_2048(padded):
+    """fp32 causal B=8 H=8 S=2048 D=64 (and the padded variant), 512 sampled rows."""
+    B, H, S, D = 8, 8, 2048, 64
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=21)
+    kv_len = inputs.padding_kv_len(B, S) if padded else None
+    o = _gpu_attn(q, k, v, True, kv_len=kv_len).cpu()
+    rows = inputs.sample_rows(B, H, S, n=512, seed=22, forced=(0, 127, 128, 1535, 1536, 2047))
+    want = oracle.attn_rows(q, k, v, rows, causal=True, kv_len=kv_len)
+    assert_close(_sampled(o, rows), want, torch.float32, "fp32 causal 2048")
+
+
+def test_workload_bf16_causal_4096():
+    """bf16 causal B=4 H=16 S=4096 D=128, 256 sampled rows."""
+    B, H, S, D = 4, 16, 4096, 128
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=31)
+    o = _gpu_attn(q, k, v, True).cpu()
+    rows = inputs.sample_rows(B, H, S, n=256, seed=32, forced=(0, 255, 256, 4095))
+    want = oracle.attn_rows(q, k, v, rows, causal=True)
+    assert_close(_sampled(o, rows), want, torch.bfloat16, "bf16 causal 4096")
