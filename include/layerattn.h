@@ -68,7 +68,7 @@ typedef enum {
 typedef enum { LA_F32 = 0, LA_BF16 = 1, LA_F16 = 2 } la_dtype;
 
 /* Operation codes for la_workspace_size(). */
-typedef enum { LA_OP_ATTN_FWD = 0, LA_OP_ATTN_CHUNKED = 1, LA_OP_LAYER_ATTN = 2 } la_op;
+typedef enum { LA_OP_ATTN_FWD = 0, LA_OP_ATTN_CHUNKED = 1, LA_OP_LAYER_ATTN = 2, LA_OP_QKV_PROJ = 3 } la_op;
 
 /*
  * Growing key/value cache for the chunked mode.  k and v are caller-owned
@@ -94,12 +94,17 @@ typedef struct {
  *   q,k,v [B, H, S, D] outputs       y = x.Wqkv + bqkv split per head; q is
  *                                    further multiplied by q_scale
  * d_model must be H*D with D in {64, 128}.  S >= 0 (S == 0 is a no-op).
- * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED or LA_ERR_CUDA.
+ * ws, ws_bytes: workspace of la_workspace_size(LA_OP_QKV_PROJ, B, H, S, S,
+ *   D, dt) bytes; fp32 needs 3*d_model*d_model*4 bytes there (the TF32
+ *   tensor cores take K-major operands only, so the weight is transposed
+ *   into it first), bf16/fp16 need none (ws may be NULL).
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE or
+ * LA_ERR_CUDA.
  */
 la_status la_qkv_proj(const void *x, const void *Wqkv, const void *bqkv,
                       void *q, void *k, void *v,
                       int B, int S, int d_model, int H, float q_scale,
-                      la_dtype dt, la_stream_t st);
+                      la_dtype dt, void *ws, size_t ws_bytes, la_stream_t st);
 
 /*
  * Attention forward ("Shape-Aware Attention", section Inspiration, the
@@ -107,14 +112,18 @@ la_status la_qkv_proj(const void *x, const void *Wqkv, const void *bqkv,
  * Layer", section What we learned).
  *   q [B, H, S_q, D]; k, v [B, H, S_kv, D]; o [B, H, S_q, D] output.
  *   causal, scale, kv_len: see the conventions above.
- *   ws, ws_bytes: optional workspace.  With at least
+ *   ws, ws_bytes: workspace.  With at least
  *     la_workspace_size(LA_OP_ATTN_FWD, ...) bytes the call may split long
  *     key ranges across thread blocks and merge the partial results
- *     (split-KV); with less (or NULL) it runs unsplit.  Results agree to
- *     rounding either way.
+ *     (split-KV); with less it runs unsplit.  Results agree to rounding
+ *     either way.  bf16/fp16 need no workspace (ws may be NULL).  fp32 needs
+ *     at least B*H*D*round_up(S_kv, 4)*4 bytes (rounded up to 256): V is
+ *     transposed there first, because the TF32 tensor cores take K-major
+ *     operands only; with less the call returns LA_ERR_WORKSPACE.
  * S_q == 0 is a no-op; S_kv == 0 writes zero rows.  q and o may be NULL
  * only when S_q == 0, k and v only when S_kv == 0.
- * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED or LA_ERR_CUDA.
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE or
+ * LA_ERR_CUDA.
  */
 la_status la_attn_fwd(const void *q, const void *k, const void *v, void *o,
                       int B, int H, int S_q, int S_kv, int D, int causal, float scale,
@@ -132,7 +141,8 @@ la_status la_attn_fwd(const void *q, const void *k, const void *v, void *o,
  * cache->len grows by chunk.  Calling it window after window over a sequence
  * gives the same result as attending the whole sequence at once.
  * cache->len + chunk must not exceed cache->S_max; cache->dtype, B, H and D
- * describe all five tensors.  ws: as for la_attn_fwd, sized with
+ * describe all five tensors.  ws: as for la_attn_fwd (fp32 transposes the
+ * cache's valid V rows into it on every call), sized with
  * la_workspace_size(LA_OP_ATTN_CHUNKED, B, H, chunk, S_max, D, dtype).
  * On any non-OK status cache->len is unchanged.
  */
@@ -147,7 +157,8 @@ la_status la_attn_chunked(const void *q_chunk, const void *k_chunk, const void *
  *   o [B, S, d_model] with head h in columns h*D .. h*D+D-1.
  * The output projection is not applied.  ws must hold at least
  * la_workspace_size(LA_OP_LAYER_ATTN, B, H, S, S, d_model / H, dt) bytes
- * (the head-major q, k, v); otherwise LA_ERR_WORKSPACE.
+ * (the head-major q, k, v; for fp32 V is kept transposed and the weight's
+ * transpose is kept too); otherwise LA_ERR_WORKSPACE.
  */
 la_status la_layer_attn(const void *x, const void *Wqkv, const void *bqkv, void *o,
                         int B, int S, int d_model, int H, int causal,
@@ -157,8 +168,8 @@ la_status la_layer_attn(const void *x, const void *Wqkv, const void *bqkv, void 
 /*
  * Workspace bytes an operation wants (0 if none).  op is an la_op; the
  * remaining arguments are those of the call (for LA_OP_ATTN_CHUNKED pass
- * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN pass
- * S_q = S_kv = S).  Returns (size_t)-1 for invalid arguments.  Host only;
+ * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN and
+ * LA_OP_QKV_PROJ pass S_q = S_kv = S and D = d_model / H).  Returns (size_t)-1 for invalid arguments.  Host only;
  * touches no device.
  */
 size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt);
@@ -170,6 +181,27 @@ size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtyp
  * LA_ERR_CUDA if the stream itself reports an error, else LA_OK.
  */
 la_status la_get_last_error(la_stream_t st);
+
+/*
+ * The raw device error word read by the latest la_get_last_error() of this
+ * process: bit 0 a bounded wait ran out, bit 1 a consistency check failed,
+ * bit 8+i wait site i gave up (0 Q loaded, 1 K loaded, 2 V loaded, 3 K slot
+ * free, 4 V slot free, 5 scores ready, 6 probabilities ready, 7 output ready,
+ * 8 projection stage loaded, 9 projection stage free, 10 projection
+ * accumulator ready).  For diagnostics; 0 when all was well.
+ */
+uint32_t la_last_error_detail(void);
+
+/*
+ * Test hook for the failure path (the pages have no counterpart).  mode 1:
+ * the next attention launch of this process issues none of its tile loads,
+ * so every consumer's bounded wait runs out (about a second); that kernel
+ * writes no output, the call itself returns LA_OK and the next
+ * la_get_last_error() returns LA_ERR_TIMEOUT, with the CUDA context intact.
+ * mode 0 withdraws a pending request.  Nothing faults, traps or hangs.
+ * Returns LA_OK, or LA_ERR_INVALID for another mode.
+ */
+la_status la_debug_inject_timeout(int mode);
 
 /* Static, human-readable name of a status. */
 const char *la_status_string(la_status s);

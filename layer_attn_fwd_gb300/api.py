@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "liblayerattn.so")
 
 LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_INTERNAL = range(7)
 LA_F32, LA_BF16, LA_F16 = 0, 1, 2
-LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN = 0, 1, 2
+LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN, LA_OP_QKV_PROJ = 0, 1, 2, 3
 
 _DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16, torch.float16: LA_F16}
 
@@ -51,13 +51,17 @@ def load(path: str | None = None):
             raise RuntimeError(f"liblayerattn.so not built ({path}); run layer_attn_fwd_gb300.build.build()")
         lib = ctypes.CDLL(path)
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        lib.la_qkv_proj.argtypes = [P, P, P, P, P, P, I, I, I, I, F, I, P]
+        lib.la_qkv_proj.argtypes = [P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
         lib.la_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, I, P, Z, P]
         lib.la_attn_chunked.argtypes = [P, P, P, ctypes.POINTER(la_kv_cache), P, I, I, F, P, Z, P]
         lib.la_layer_attn.argtypes = [P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
         lib.la_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.la_workspace_size.restype = Z
         lib.la_get_last_error.argtypes = [P]
+        lib.la_last_error_detail.argtypes = []
+        lib.la_last_error_detail.restype = ctypes.c_uint32
+        lib.la_debug_inject_timeout.argtypes = [I]
+        lib.la_debug_inject_timeout.restype = I
         lib.la_status_string.argtypes = [I]
         lib.la_status_string.restype = ctypes.c_char_p
         for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_get_last_error"):
@@ -115,7 +119,7 @@ def _workspace(nbytes, device, ws):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def qkv_proj(x, Wqkv, bqkv, H, q_scale=1.0, out=None, stream=None):
+def qkv_proj(x, Wqkv, bqkv, H, q_scale=1.0, out=None, workspace=None, stream=None):
     """x [B,S,d], Wqkv [d,3d], bqkv [3d] or None -> q, k, v [B,H,S,D]."""
     for t, n in ((x, "x"), (Wqkv, "Wqkv")):
         _need(t, n)
@@ -126,9 +130,19 @@ def qkv_proj(x, Wqkv, bqkv, H, q_scale=1.0, out=None, stream=None):
     if out is None:
         out = tuple(torch.empty(B, H, S, D, dtype=x.dtype, device=x.device) for _ in range(3))
     q, k, v = out
+    if workspace is None and D in (64, 128) and x.dtype in _DT:
+        workspace = _workspace(workspace_size(LA_OP_QKV_PROJ, B, H, S, S, D, x.dtype), x.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().la_qkv_proj(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(q), _ptr(k), _ptr(v), B, S, dm, H,
-                              float(q_scale), _dt(x), _stream(stream)), "la_qkv_proj")
+                              float(q_scale), _dt(x), _ptr(workspace), nbytes, _stream(stream)), "la_qkv_proj")
     return q, k, v
+
+
+def fp32_vt_bytes(B, H, S_kv, D):
+    """Workspace an fp32 attention call needs at least (V transposed for the
+    TF32 tensor cores): B*H*D*round_up(S_kv, 4)*4 rounded up to 256."""
+    n = B * H * D * ((S_kv + 3) // 4 * 4) * 4
+    return (n + 255) // 256 * 256
 
 
 def attn_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, workspace=None, stream=None):
@@ -199,6 +213,17 @@ def layer_attn(x, Wqkv, bqkv, H, causal=False, kv_len=None, out=None, workspace=
     _check(load().la_layer_attn(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(o), B, S, dm, H, int(bool(causal)),
                                 _ptr(kv_len), _dt(x), _ptr(workspace), nbytes, _stream(stream)), "la_layer_attn")
     return o
+
+
+def last_error_detail() -> int:
+    """Raw device error word seen by the latest get_last_error()."""
+    return int(load().la_last_error_detail())
+
+
+def debug_inject_timeout(mode=1):
+    """Test hook: the next attention launch skips its loads so its bounded
+    waits run out and get_last_error() reports LA_ERR_TIMEOUT."""
+    _check(load().la_debug_inject_timeout(int(mode)), "la_debug_inject_timeout")
 
 
 def get_last_error(stream=None) -> int:

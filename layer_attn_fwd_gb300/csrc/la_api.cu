@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "la_device.cuh"
@@ -46,6 +47,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 constexpr int kMaxDevices = 64;
 
+// One-shot request from la_debug_inject_timeout().
+std::atomic<int> g_skip_loads_once{0};
+// Raw device error word seen by the latest la_get_last_error().
+std::atomic<uint32_t> g_last_word{0};
+
 uint32_t* error_word() {
   static std::mutex mu;
   static uint32_t* addr[kMaxDevices] = {};
@@ -72,22 +78,29 @@ CUtensorMapDataType tma_type(la_dtype dt) {
                       : (dt == LA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 }
 
-// 4-D map over a [B, H, rows, D] view (strides in elements), 128-byte swizzle.
-la_status map_bhsd(CUtensorMap* m, const void* base, la_dtype dt, int B, int H, long long rows, int D,
-                   long long s_row, long long s_head, long long s_batch, int box_rows, int box_cols) {
+// 4-D tiled map, 128-byte swizzle: extents d0 (innermost, contiguous) .. d3,
+// strides s1..s3 in elements, box box0 x box1 x 1 x 1.
+la_status map_4d(CUtensorMap* m, const void* base, la_dtype dt, long long d0, long long d1, long long d2,
+                 long long d3, long long s1, long long s2, long long s3, int box0, int box1) {
   auto fn = encode_fn();
   if (fn == nullptr) return LA_ERR_CUDA;
   const long long e = elem_bytes(dt);
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows > 0 ? rows : 1),
-                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row * e), static_cast<cuuint64_t>(s_head * e),
-                           static_cast<cuuint64_t>(s_batch * e)};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d0 > 0 ? d0 : 1), static_cast<cuuint64_t>(d1 > 0 ? d1 : 1),
+                        static_cast<cuuint64_t>(d2), static_cast<cuuint64_t>(d3)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s1 * e), static_cast<cuuint64_t>(s2 * e),
+                           static_cast<cuuint64_t>(s3 * e)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, tma_type(dt), 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LA_OK : LA_ERR_CUDA;
+}
+
+// [B, H, rows, D] view with the given element strides.
+la_status map_bhsd(CUtensorMap* m, const void* base, la_dtype dt, int B, int H, long long rows, int D,
+                   long long s_row, long long s_head, long long s_batch, int box_rows, int box_cols) {
+  return map_4d(m, base, dt, D, rows, H, B, s_row, s_head, s_batch, box_cols, box_rows);
 }
 
 // 2-D map over a row-major [rows, cols] matrix.
@@ -121,6 +134,18 @@ size_t split_bytes(int splits, int B, int H, int S_q, int D) {
   if (splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(splits) * B * H * S_q;
   return round_up(rows * D * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+
+// fp32 only: V^T [B, H, D, S_pad] for the TF32 PV product (K-major operands).
+long long vt_pad(long long S_kv) { return (S_kv + 3) / 4 * 4; }
+size_t vt_bytes(la_dtype dt, int B, int H, long long S_kv, int D) {
+  if (dt != LA_F32) return 0;
+  return round_up(static_cast<size_t>(B) * H * D * vt_pad(S_kv) * 4, 256);
+}
+// fp32 only: Wqkv^T [3d, d] for the TF32 projection.
+size_t wt_bytes(la_dtype dt, int d_model) {
+  if (dt != LA_F32) return 0;
+  return round_up(static_cast<size_t>(3) * d_model * d_model * 4, 256);
 }
 
 // Split the key range only when the unsplit grid leaves the GPU short of
@@ -166,16 +191,41 @@ la_status check_attn_args(int B, int H, int S_q, int S_kv, int D, float scale, i
   return LA_OK;
 }
 
-// Attention over views: q [B,H,S_q,D] contiguous; k/v rows [0, S_kv) of a
-// [B,H,kv_rows_alloc,D] buffer; o with the given element strides.
-la_status run_attention(const void* q, const void* k, const void* v, long long kv_rows_alloc, void* o,
-                        long long o_sb, long long o_sh, long long o_ss, int B, int H, int S_q, int S_kv, int D,
-                        int causal, float scale, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes,
-                        cudaStream_t st) {
+// Key/value operands of one attention call: rows [0, S_kv) of k/v buffers
+// [B, H, rows_alloc, D]; for fp32 V may instead be given already transposed
+// as V^T [B, H, D, vt_ld] (vt != nullptr).
+struct KVView {
+  const void* k;
+  const void* v;
+  long long rows_alloc;
+  const void* vt;
+  long long vt_ld;
+};
+
+// Attention: q [B,H,S_q,D] contiguous; o with the given element strides.
+// Scratch from ws: the fp32 V^T (unless given), then the split partials.
+la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb, long long o_sh, long long o_ss,
+                        int B, int H, int S_q, int S_kv, int D, int causal, float scale, const int32_t* kv_len,
+                        la_dtype dt, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (S_q == 0) return LA_OK;
   AttnShape sh;
   if (!attn_shape(dt, D, &sh)) return LA_ERR_UNSUPPORTED;
-  const Plan p = make_plan(dt, B, H, S_q, S_kv, D, ws == nullptr ? 0 : ws_bytes, device_sms());
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  size_t w_left = ws == nullptr ? 0 : ws_bytes;
+  const void* vt = kv.vt;
+  long long vt_ld = kv.vt_ld;
+  if (dt == LA_F32 && vt == nullptr) {
+    const size_t need = vt_bytes(dt, B, H, S_kv, D);
+    if (w_left < need) return LA_ERR_WORKSPACE;
+    vt_ld = vt_pad(S_kv);
+    if (S_kv > 0 && launch_transpose32(kv.v, kv.rows_alloc * D, w, vt_ld, static_cast<long long>(B) * H, S_kv, D,
+                                       st) != cudaSuccess)
+      return LA_ERR_CUDA;
+    vt = w;
+    w += need;
+    w_left -= need;
+  }
+  const Plan p = make_plan(dt, B, H, S_q, S_kv, D, w_left, device_sms());
   uint32_t* err = error_word();
   if (err == nullptr) return LA_ERR_CUDA;
   CUtensorMap tq, tk, tv;
@@ -183,11 +233,17 @@ la_status run_attention(const void* q, const void* k, const void* v, long long k
   s = map_bhsd(&tq, q, dt, B, H, S_q, D, D, static_cast<long long>(S_q) * D, static_cast<long long>(H) * S_q * D,
                sh.box_q_rows, sh.box_cols);
   if (s != LA_OK) return s;
-  s = map_bhsd(&tk, k, dt, B, H, S_kv, D, D, kv_rows_alloc * D, static_cast<long long>(H) * kv_rows_alloc * D,
+  s = map_bhsd(&tk, kv.k, dt, B, H, S_kv, D, D, kv.rows_alloc * D, static_cast<long long>(H) * kv.rows_alloc * D,
                sh.box_kv_rows, sh.box_cols);
   if (s != LA_OK) return s;
-  s = map_bhsd(&tv, v, dt, B, H, S_kv, D, D, kv_rows_alloc * D, static_cast<long long>(H) * kv_rows_alloc * D,
-               sh.box_kv_rows, sh.box_cols);
+  if (dt == LA_F32) {
+    // V^T: keys innermost (the K dimension of the PV product), head dims as rows
+    s = map_4d(&tv, vt, dt, S_kv, D, H, B, vt_ld, static_cast<long long>(D) * vt_ld,
+               static_cast<long long>(H) * D * vt_ld, sh.box_cols, D);
+  } else {
+    s = map_bhsd(&tv, kv.v, dt, B, H, S_kv, D, D, kv.rows_alloc * D, static_cast<long long>(H) * kv.rows_alloc * D,
+                 sh.box_kv_rows, sh.box_cols);
+  }
   if (s != LA_OK) return s;
 
   AttnArgs a;
@@ -206,10 +262,11 @@ la_status run_attention(const void* q, const void* k, const void* v, long long k
   a.num_qblk = p.num_qblk;
   a.tiles_per_split = p.tiles_per_split;
   a.err = err;
+  a.skip_loads = g_skip_loads_once.exchange(0);
   if (p.splits > 1) {
     const size_t rows = static_cast<size_t>(p.splits) * B * H * S_q;
-    a.part_o = static_cast<float*>(ws);
-    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round_up(rows * D * sizeof(float), 256));
+    a.part_o = reinterpret_cast<float*>(w);
+    a.part_lse = reinterpret_cast<float*>(w + round_up(rows * D * sizeof(float), 256));
   }
   cudaError_t e = launch_attn(dt, D, tq, tk, tv, a, p.splits, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
@@ -232,6 +289,12 @@ la_status run_attention(const void* q, const void* k, const void* v, long long k
   return LA_OK;
 }
 
+size_t attn_ws_bytes(la_dtype dt, int B, int H, int S_q, int S_kv, int D, bool need_vt) {
+  if (S_q == 0) return 0;
+  const size_t vt = need_vt ? vt_bytes(dt, B, H, S_kv, D) : 0;
+  return vt + make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), device_sms()).ws_bytes;
+}
+
 la_status check_proj_args(const void* x, const void* W, const void* bias, const void* q, const void* k,
                           const void* v, int B, int S, int d_model, int H, float q_scale, int dt) {
   if (!x || !W || !q || !k || !v) return LA_ERR_INVALID;
@@ -246,8 +309,11 @@ la_status check_proj_args(const void* x, const void* W, const void* bias, const 
   return LA_OK;
 }
 
+// Projection; scratch from ws: the fp32 Wqkv^T.  With vt != nullptr (fp32
+// sublayer) V is written as V^T [B, H, D, vt_ld] there instead of into v.
 la_status run_proj(const void* x, const void* W, const void* bias, void* q, void* k, void* v, int B, int S,
-                   int d_model, int H, float q_scale, la_dtype dt, cudaStream_t st) {
+                   int d_model, int H, float q_scale, la_dtype dt, void* ws, size_t ws_bytes, void* vt,
+                   long long vt_ld, cudaStream_t st) {
   const long long M = static_cast<long long>(B) * S;
   if (M == 0) return LA_OK;
   ProjShape ps;
@@ -257,13 +323,21 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   CUtensorMap tx, tw;
   la_status s = map_2d(&tx, x, dt, M, d_model, kTileM, ps.box_cols);
   if (s != LA_OK) return s;
-  s = map_2d(&tw, W, dt, d_model, 3LL * d_model, ps.box_k_rows, ps.box_cols);
+  if (ps.w_transposed) {
+    const size_t need = wt_bytes(dt, d_model);
+    if (ws == nullptr || ws_bytes < need) return LA_ERR_WORKSPACE;
+    if (launch_transpose32(W, 0, ws, d_model, 1, d_model, 3 * d_model, st) != cudaSuccess) return LA_ERR_CUDA;
+    s = map_2d(&tw, ws, dt, 3LL * d_model, d_model, ps.block_n, ps.box_cols);
+  } else {
+    s = map_2d(&tw, W, dt, d_model, 3LL * d_model, ps.box_k_rows, ps.box_cols);
+  }
   if (s != LA_OK) return s;
   ProjArgs a;
+  memset(&a, 0, sizeof a);
   a.bias = bias;
   a.q = q;
   a.k = k;
-  a.v = v;
+  a.v = vt != nullptr ? vt : v;
   a.M = static_cast<int>(M);
   a.N = 3 * d_model;
   a.K = d_model;
@@ -272,6 +346,8 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   a.D = d_model / H;
   a.q_scale = q_scale;
   a.err = err;
+  a.v_transposed = vt != nullptr;
+  a.S_pad = vt_ld;
   return cuda_status(launch_proj(dt, tx, tw, a, st));
 }
 
@@ -287,10 +363,13 @@ using namespace la;
 extern "C" {
 
 la_status la_qkv_proj(const void* x, const void* Wqkv, const void* bqkv, void* q, void* k, void* v, int B, int S,
-                      int d_model, int H, float q_scale, la_dtype dt, la_stream_t st) {
+                      int d_model, int H, float q_scale, la_dtype dt, void* ws, size_t ws_bytes, la_stream_t st) {
   la_status s = check_proj_args(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt);
   if (s != LA_OK) return s;
-  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, reinterpret_cast<cudaStream_t>(st));
+  if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
+  if (S > 0 && (ws == nullptr ? 0 : ws_bytes) < wt_bytes(dt, d_model)) return LA_ERR_WORKSPACE;
+  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, ws, ws_bytes, nullptr, 0,
+                  reinterpret_cast<cudaStream_t>(st));
 }
 
 la_status la_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int S_q, int S_kv,
@@ -306,9 +385,10 @@ la_status la_attn_fwd(const void* q, const void* k, const void* v, void* o, int 
   if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
   if (S_q == 0) return LA_OK;
   if (S_kv == 0) k = v = q;  // no key is ever loaded; the maps only need a valid base
-  return run_attention(q, k, v, S_kv, o, static_cast<long long>(H) * S_q * D, static_cast<long long>(S_q) * D, D,
-                       B, H, S_q, S_kv, D, causal, scale, kv_len, dt, ws, ws_bytes,
-                       reinterpret_cast<cudaStream_t>(st));
+  if ((ws == nullptr ? 0 : ws_bytes) < vt_bytes(dt, B, H, S_kv, D)) return LA_ERR_WORKSPACE;
+  const KVView kv{k, v, S_kv, nullptr, 0};
+  return run_attention(q, kv, o, static_cast<long long>(H) * S_q * D, static_cast<long long>(S_q) * D, D, B, H,
+                       S_q, S_kv, D, causal, scale, kv_len, dt, ws, ws_bytes, reinterpret_cast<cudaStream_t>(st));
 }
 
 la_status la_attn_chunked(const void* q_chunk, const void* k_chunk, const void* v_chunk, la_kv_cache* cache,
@@ -326,14 +406,15 @@ la_status la_attn_chunked(const void* q_chunk, const void* k_chunk, const void* 
   if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
   if (chunk == 0) return LA_OK;
   const la_dtype dt = cache->dtype;
+  const int S_kv = cache->len + chunk;
+  if ((ws == nullptr ? 0 : ws_bytes) < vt_bytes(dt, B, H, S_kv, D)) return LA_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
   if (launch_kv_append(k_chunk, v_chunk, cache->k, cache->v, B, H, chunk, D, cache->S_max, cache->len,
                        elem_bytes(dt), cs) != cudaSuccess)
     return LA_ERR_CUDA;
-  const int S_kv = cache->len + chunk;
-  s = run_attention(q_chunk, cache->k, cache->v, cache->S_max, o_chunk, static_cast<long long>(H) * chunk * D,
-                    static_cast<long long>(chunk) * D, D, B, H, chunk, S_kv, D, causal, scale, nullptr, dt, ws,
-                    ws_bytes, cs);
+  const KVView kv{cache->k, cache->v, cache->S_max, nullptr, 0};
+  s = run_attention(q_chunk, kv, o_chunk, static_cast<long long>(H) * chunk * D, static_cast<long long>(chunk) * D,
+                    D, B, H, chunk, S_kv, D, causal, scale, nullptr, dt, ws, ws_bytes, cs);
   if (s == LA_OK) cache->len = S_kv;
   return s;
 }
@@ -350,34 +431,41 @@ la_status la_layer_attn(const void* x, const void* Wqkv, const void* bqkv, void*
   s = check_attn_args(B, H, S, S, D, 1.f, dt);
   if (s != LA_OK) return s;
   if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return LA_ERR_INVALID;
+  // ws: q | k | v (fp32: V^T [B,H,D,S_pad]) | fp32 Wqkv^T | split partials
   const size_t one = layer_qkv_bytes(B, S, d_model, dt);
-  if (ws_bytes < 3 * one) return LA_ERR_WORKSPACE;
+  const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S, D) : one;
+  const size_t fixed = 2 * one + vbytes + wt_bytes(dt, d_model);
+  if (ws_bytes < fixed) return LA_ERR_WORKSPACE;
   if (S == 0) return LA_OK;
   uint8_t* w = static_cast<uint8_t*>(ws);
   void *q = w, *k = w + one, *v = w + 2 * one;
+  uint8_t* wt = w + 2 * one + vbytes;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
-  s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, cs);
+  const bool vt = dt == LA_F32;
+  s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, wt, wt_bytes(dt, d_model), vt ? v : nullptr,
+               vt_pad(S), cs);
   if (s != LA_OK) return s;
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  return run_attention(q, k, v, S, o, static_cast<long long>(S) * d_model, D, d_model, B, H, S, S, D, causal,
-                       scale, kv_len, dt, w + 3 * one, ws_bytes - 3 * one, cs);
+  const KVView kv{k, v, S, vt ? v : nullptr, vt_pad(S)};
+  return run_attention(q, kv, o, static_cast<long long>(S) * d_model, D, d_model, B, H, S, S, D, causal, scale,
+                       kv_len, dt, w + fixed, ws_bytes - fixed, cs);
 }
 
 size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt) {
   const size_t bad = static_cast<size_t>(-1);
   if (check_attn_args(B, H, S_q, S_kv, D, 1.f, dt) != LA_OK) return bad;
-  const int sms = device_sms();
   switch (op) {
     case LA_OP_ATTN_FWD:
     case LA_OP_ATTN_CHUNKED:
-      if (S_q == 0) return 0;
-      return make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), sms).ws_bytes;
+      return attn_ws_bytes(dt, B, H, S_q, S_kv, D, true);
     case LA_OP_LAYER_ATTN: {
       if (S_q != S_kv) return bad;
-      const size_t qkv = 3 * layer_qkv_bytes(B, S_q, H * D, dt);
-      if (S_q == 0) return qkv;
-      return qkv + make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), sms).ws_bytes;
+      const size_t one = layer_qkv_bytes(B, S_q, H * D, dt);
+      const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S_q, D) : one;
+      return 2 * one + vbytes + wt_bytes(dt, H * D) + attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);
     }
+    case LA_OP_QKV_PROJ:
+      return wt_bytes(dt, H * D);
     default:
       return bad;
   }
@@ -388,12 +476,21 @@ la_status la_get_last_error(la_stream_t st) {
   if (e != cudaSuccess) return LA_ERR_CUDA;
   uint32_t w = 0;
   if (cudaMemcpyFromSymbol(&w, la_device_error_word, sizeof w) != cudaSuccess) return LA_ERR_CUDA;
+  g_last_word.store(w);
   if (w != 0) {
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbol(la_device_error_word, &zero, sizeof zero) != cudaSuccess) return LA_ERR_CUDA;
   }
   if (w & DEVERR_TIMEOUT) return LA_ERR_TIMEOUT;
   if (w & DEVERR_INTERNAL) return LA_ERR_INTERNAL;
+  return LA_OK;
+}
+
+uint32_t la_last_error_detail(void) { return g_last_word.load(); }
+
+la_status la_debug_inject_timeout(int mode) {
+  if (mode != 0 && mode != 1) return LA_ERR_INVALID;
+  g_skip_loads_once.store(mode);
   return LA_OK;
 }
 

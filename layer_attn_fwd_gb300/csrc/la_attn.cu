@@ -12,6 +12,8 @@
 //
 //   warp 4*NQ   (TMA)      loads Q once, then K_j / V_j through an NS-stage
 //                          ring of shared-memory buffers (128-byte swizzle).
+//                          For fp32 (TF32 products, which take K-major
+//                          operands only) V comes from its transpose V^T.
 //   warp 4*NQ+1 (MMA)      one thread issues tcgen05.mma:  S_t = Q_t K_j^T into
 //                          tensor memory, then O_t += P_t V_j with P_t read
 //                          straight from tensor memory (A operand in TMEM).
@@ -98,6 +100,10 @@ struct Cfg {
   static constexpr int QK_STEPS = D * E / 32;              // one MMA consumes 32 bytes of a row
   static constexpr int PV_ROWS = 32 / E;                   // keys per PV MMA (16, or 8 for tf32)
   static constexpr int PV_STEPS = BN / PV_ROWS;
+  // TF32 takes K-major operands only: V then arrives transposed (V^T rows are
+  // head dims, keys contiguous) and a V tile is BN*E/128 chunks of D rows.
+  static constexpr bool VT = (E == 4);
+  static constexpr int VT_CHUNK = D * 128;
   static constexpr int THREADS = NQ * 128 + 64;
   static constexpr int WARP_TMA = NQ * 4;
   static constexpr int WARP_MMA = NQ * 4 + 1;
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
 #pragma unroll
     for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
     bool q_issued = false;
-    if (lane == 0 && je_all > jb) {
+    if (lane == 0 && je_all > jb && !a.skip_loads) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -263,17 +269,23 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
       q_issued = true;
       for (int j = jb; j < je_all; ++j) {
         const int i = j - jb, s = i % NS, r = i / NS;
-        if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab)) break;
+        if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab, SITE_K_EMPTY)) break;
         mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_4d(&tm_k, &k_full[s], smem + C::OFF_K + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
                       j * BN, h, b, pol_kv);
         last_k[s] = r;
-        if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab)) break;
+        if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab, SITE_V_EMPTY)) break;
         mbar_arrive_expect_tx(&v_full[s], C::KV_TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(&tm_v, &v_full[s], smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
-                      j * BN, h, b, pol_kv);
+        if constexpr (C::VT) {
+          for (int c = 0; c < BN / C::CW; ++c)
+            tma_load_4d(&tm_v, &v_full[s], smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW,
+                        0, h, b, pol_kv);
+        } else {
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d(&tm_v, &v_full[s], smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
+                        j * BN, h, b, pol_kv);
+        }
         last_v[s] = r;
       }
     }
@@ -292,7 +304,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
     // ======================= MMA issuer ====================================
     if (lane == 0 && je_all > jb) {
       const uint32_t idesc_qk = idesc_make(Elem<T>::ab, kTileM, BN, false, false);
-      const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, true);
+      const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, !C::VT);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
@@ -308,18 +320,23 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
           mma_ss<TF32>(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_t V_j: P from tensor memory, V MN-major (rows = keys).
+      // O_t += P_t V_j: P from tensor memory; V MN-major (rows = keys), or for
+      // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step).
       auto issue_pv = [&](int t, int j) {
         const int s = (j - jb) % NS;
         const uint32_t d = tmem + t * C::TILE_COLS + BN;
         const uint32_t p = tmem + t * C::TILE_COLS;
 #pragma unroll
         for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-          const uint64_t bd = sdesc_sw128(sV + s * C::KV_TILE + kk * C::PV_ROWS * 128, C::KV_CHUNK, 1024);
+          uint64_t bd;
+          if constexpr (C::VT)
+            bd = sdesc_sw128(sV + s * C::KV_TILE + (kk >> 2) * C::VT_CHUNK + (kk & 3) * 32, 16, 1024);
+          else
+            bd = sdesc_sw128(sV + s * C::KV_TILE + kk * C::PV_ROWS * 128, C::KV_CHUNK, 1024);
           mma_ts<TF32>(d, p + kk * 8, bd, idesc_pv, (j > jb || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(q_full, 0, ab) && mbar_wait(&k_full[0], 0, ab);
+      bool ok = mbar_wait(q_full, 0, ab, SITE_Q_FULL) && mbar_wait(&k_full[0], 0, ab, SITE_K_FULL);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < NQ; ++t) {
@@ -336,16 +353,16 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
         bool v_ready = false, k_next = false;
         for (int t = 0; t < NQ && ok; ++t) {
           if (j >= je[t]) continue;
-          if (!mbar_wait(&p_full[t], i & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(&p_full[t], i & 1, ab, SITE_P_FULL)) { ok = false; break; }
           if (!v_ready) {
-            if (!mbar_wait(&v_full[s], r & 1, ab)) { ok = false; break; }
+            if (!mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL)) { ok = false; break; }
             v_ready = true;
           }
           tc_fence_after();
           issue_pv(t, j);
           if (j + 1 < je[t]) {
             if (!k_next) {
-              if (!mbar_wait(&k_full[sn], rn & 1, ab)) { ok = false; break; }
+              if (!mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL)) { ok = false; break; }
               tc_fence_after();
               k_next = true;
             }
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
     bool ok = true;
     for (int j = jb; j < je[t]; ++j) {
       const int i = j - jb;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], i & 1, ab));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], i & 1, ab, SITE_S_FULL));
       if (!ok) break;
       tc_fence_after();
       uint32_t s[BN];
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
     }
     const bool has_o = je[t] > jb;
     if (ok && has_o) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, ab));
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, ab, SITE_O_FULL));
       if (ok) tc_fence_after();
     }
     if (ok) {

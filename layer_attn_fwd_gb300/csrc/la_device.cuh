@@ -59,17 +59,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Wait sites, recorded as bit (8 + site) of the error word when a wait runs out.
+enum WaitSite : uint32_t {
+  SITE_Q_FULL = 0, SITE_K_FULL, SITE_V_FULL, SITE_K_EMPTY, SITE_V_EMPTY, SITE_S_FULL, SITE_P_FULL,
+  SITE_O_FULL, SITE_PROJ_FULL, SITE_PROJ_EMPTY, SITE_PROJ_ACC
+};
+
 // Wait until the phase with the given parity has completed.  Returns false
-// (after latching the error) when the limit runs out or another thread of the
-// CTA has already given up; the caller must then stop its role.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab) {
+// (after latching the error and the site) when the limit runs out or another
+// thread of the CTA has already given up; the caller must then stop its role.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
-      atomicOr(ab.err, DEVERR_TIMEOUT);
+      atomicOr(ab.err, DEVERR_TIMEOUT | (1u << (8 + site)));
       *ab.flag = 1;
       return false;
     }

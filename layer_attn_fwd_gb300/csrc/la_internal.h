@@ -26,6 +26,7 @@ struct AttnArgs {
   int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
   int tiles_per_split;        // key tiles handled by one split
   uint32_t* err;              // device error word
+  int skip_loads;             // test hook: issue no TMA load, so every wait runs out
 };
 
 // Static launch shape of the attention kernel for a dtype and head dim.
@@ -52,6 +53,12 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st);
 
+// Batched transpose of 4-byte elements: dst[b][c][r] = src[b][r][c]; source
+// rows of C elements, batches src_batch apart; destination rows of ld_dst
+// elements, batches C*ld_dst apart.
+cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
+                               int R, int C, cudaStream_t st);
+
 // Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`.
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
                              int rows, int D, int S_max, int at, int elem_bytes, cudaStream_t st);
@@ -66,11 +73,14 @@ struct ProjArgs {
   int S, H, D;
   float q_scale;
   uint32_t* err;
+  int v_transposed;   // write V as V^T [B, H, D, S_pad] (fp32 sublayer) instead of [B, H, S, D]
+  long long S_pad;    // row length of V^T
 };
 struct ProjShape {
   int block_n;        // output columns per CTA
   int box_cols;       // TMA box columns (one 128-byte swizzle row)
   int box_k_rows;     // TMA box rows of the weight tile (= K per stage)
+  bool w_transposed;  // the weight is read as Wqkv^T [3d, d] (TF32: K-major only)
 };
 bool proj_shape(la_dtype dt, ProjShape* s);
 cudaError_t launch_proj(la_dtype dt, const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a,

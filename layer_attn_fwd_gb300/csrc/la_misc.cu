@@ -4,8 +4,11 @@
 //       o = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M),  M = max_s lse_s,
 //     the same rescaling algebra the online softmax applies tile by tile;
 //   - key/value cache append for the chunked long-context mode ("Roofline",
-//     section How we built it: windows against a growing key/value cache).
-// Both are plain coalesced 16-byte streams with grids sized to the SM count.
+//     section How we built it: windows against a growing key/value cache);
+//   - a 32-bit batched transpose: the TF32 tensor cores take K-major operands
+//     only, so fp32 V (and the fp32 projection weight) are presented
+//     transposed.
+// All are plain coalesced streams with grids sized to the SM count.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -84,6 +87,30 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// dst[b][c][r] = src[b][r][c] for 4-byte elements; source rows are C long
+// and batches src_batch apart; destination rows are ld_dst long (>= R) and
+// batches C * ld_dst apart.  32x32 tiles through shared memory, both sides
+// coalesced.
+__global__ void __launch_bounds__(256)
+    transpose32_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst, int R, int C, long long ld_dst,
+                       long long src_batch, long long dst_batch) {
+  __shared__ uint32_t tile[32][33];
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const long long b = blockIdx.z;
+  const uint32_t* s = src + b * src_batch;
+  uint32_t* d = dst + b * dst_batch;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + tx;
+    if (r < R && c < C) tile[i][tx] = s[static_cast<long long>(r) * C + c];
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + tx;
+    if (r < R && c < C) d[static_cast<long long>(c) * ld_dst + r] = tile[tx][i];
+  }
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -105,6 +132,16 @@ cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
     case LA_F16: combine_kernel<__half><<<grid, 256, 0, st>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
+                               int R, int C, cudaStream_t st) {
+  if (batches == 0 || R == 0 || C == 0) return cudaSuccess;
+  if (batches > 65535 || (C + 31) / 32 > 65535) return cudaErrorInvalidValue;
+  dim3 grid((R + 31) / 32, (C + 31) / 32, static_cast<unsigned>(batches));
+  transpose32_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(src), reinterpret_cast<uint32_t*>(dst), R,
+                                            C, ld_dst, src_batch, static_cast<long long>(C) * ld_dst);
   return cudaGetLastError();
 }
 

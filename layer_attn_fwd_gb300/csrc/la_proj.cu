@@ -10,6 +10,8 @@
 //
 //   warp 4        TMA: x tile (K-major) and Wqkv tile (rows = K, columns = N,
 //                 i.e. the B operand is MN-major) through an NSP-stage ring.
+//                 TF32 products take K-major operands only, so for fp32 the
+//                 weight is read from its transpose Wqkv^T [3d, d].
 //   warp 5        one thread issues the MMAs; commits free the stages.
 //   warps 0..3    epilogue, thread r owns row r of the tile.
 #include <cuda_bf16.h>
@@ -62,8 +64,9 @@ struct PCfg {
   static constexpr int E = sizeof(T);
   static constexpr int CW = 128 / E;           // elements per 128-byte row = K per stage
   static constexpr int A_STAGE = kTileM * 128; // x tile: 128 rows x 128 bytes
-  static constexpr int B_CHUNK = CW * 128;     // CW weight rows x 128 bytes (CW columns)
-  static constexpr int B_STAGE = (BNP / CW) * B_CHUNK;
+  static constexpr bool WT = (E == 4);         // weight tile from Wqkv^T (K-major)
+  static constexpr int B_CHUNK = WT ? BNP * 128 : CW * 128;  // MN-major: CW weight rows x 128 bytes
+  static constexpr int B_STAGE = BNP * CW * E;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = NSP * A_STAGE;
   static constexpr int OFF_BAR = OFF_B + NSP * B_STAGE;
@@ -149,12 +152,16 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t pol_w = policy_evict_last();
       for (int kt = 0; kt < n_k; ++kt) {
         const int s = kt % NSP, r = kt / NSP;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, ab)) break;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, ab, SITE_PROJ_EMPTY)) break;
         mbar_arrive_expect_tx(&full[s], C::A_STAGE + C::B_STAGE);
         tma_load_2d(&tm_x, &full[s], smem + C::OFF_A + s * C::A_STAGE, kt * C::CW, tile_m * kTileM, pol_x);
-        for (int c = 0; c < BNP / C::CW; ++c)
-          tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE + c * C::B_CHUNK,
-                      tile_n * BNP + c * C::CW, kt * C::CW, pol_w);
+        if constexpr (C::WT) {
+          tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE, kt * C::CW, tile_n * BNP, pol_w);
+        } else {
+          for (int c = 0; c < BNP / C::CW; ++c)
+            tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE + c * C::B_CHUNK,
+                        tile_n * BNP + c * C::CW, kt * C::CW, pol_w);
+        }
         last[s] = r;
       }
     }
@@ -167,18 +174,20 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == C::WARP_MMA) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_make(PElem<T>::ab, kTileM, BNP, false, true);
+      const uint32_t idesc = idesc_make(PElem<T>::ab, kTileM, BNP, false, !C::WT);
       const uint32_t sA = smem_u32(smem + C::OFF_A);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
       bool ok = true;
       for (int kt = 0; kt < n_k; ++kt) {
         const int s = kt % NSP, r = kt / NSP;
-        if (!mbar_wait(&full[s], r & 1, ab)) { ok = false; break; }
+        if (!mbar_wait(&full[s], r & 1, ab, SITE_PROJ_FULL)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = sdesc_sw128(sA + s * C::A_STAGE + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sB + s * C::B_STAGE + kk * C::ROWS_PER_KSTEP * 128, C::B_CHUNK, 1024);
+          const uint64_t bd =
+              C::WT ? sdesc_sw128(sB + s * C::B_STAGE + kk * 32, 16, 1024)
+                    : sdesc_sw128(sB + s * C::B_STAGE + kk * C::ROWS_PER_KSTEP * 128, C::B_CHUNK, 1024);
           mma_ss<TF32>(tmem, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&empty[s]);
@@ -198,7 +207,7 @@ __global__ void __launch_bounds__(192, 1)
     tmem_dealloc(tmem, C::TMEM_COLS);
   } else {
     // epilogue: thread owns output row m; 32 columns at a time
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, ab));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, ab, SITE_PROJ_ACC));
     if (ok) {
       tc_fence_after();
       const int m = tile_m * kTileM + warp * 32 + lane;
@@ -225,8 +234,15 @@ __global__ void __launch_bounds__(192, 1)
           v[c] = y * mul;
         }
         if (m < a.M) {
-          T* out = reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v));
-          store32<T>(out + ((static_cast<long long>(bidx) * a.H + hh) * a.S + srow) * a.D + dd, v);
+          if (which == 2 && a.v_transposed) {
+            // V^T [B, H, D, S_pad]: lanes hold consecutive rows, so each store is coalesced
+            T* out = reinterpret_cast<T*>(a.v) + ((static_cast<long long>(bidx) * a.H + hh) * a.D + dd) * a.S_pad + srow;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) out[c * a.S_pad] = static_cast<T>(v[c]);
+          } else {
+            T* out = reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v));
+            store32<T>(out + ((static_cast<long long>(bidx) * a.H + hh) * a.S + srow) * a.D + dd, v);
+          }
         }
       }
     }
@@ -261,6 +277,7 @@ bool proj_shape(la_dtype dt, ProjShape* s) {
   s->block_n = 256;
   s->box_cols = 128 / e;
   s->box_k_rows = 128 / e;
+  s->w_transposed = (dt == LA_F32);
   return true;
 }
 

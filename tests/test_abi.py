@@ -36,6 +36,11 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_debug_hook_validates_mode(lib):
+    assert lib.la_debug_inject_timeout(7) == api.LA_ERR_INVALID
+    assert lib.la_debug_inject_timeout(0) == api.LA_OK
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert api.status_string(s).startswith("LA_")
@@ -45,6 +50,11 @@ def test_status_strings(lib):
 def _attn(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, S_q=16, S_kv=16, D=64, causal=0, scale=0.125,
           kv_len=None, dt=api.LA_BF16, ws=None, ws_bytes=0):
     return lib.la_attn_fwd(q, k, v, o, B, H, S_q, S_kv, D, causal, scale, kv_len, dt, ws, ws_bytes, None)
+
+
+def test_fp32_attention_needs_workspace(lib):
+    assert _attn(lib, dt=api.LA_F32) == api.LA_ERR_WORKSPACE
+    assert _attn(lib, dt=api.LA_F32, ws=FAKE, ws_bytes=api.fp32_vt_bytes(1, 1, 16, 64) - 1) == api.LA_ERR_WORKSPACE
 
 
 def test_attn_fwd_rejects_bad_arguments(lib):
@@ -68,13 +78,14 @@ def test_attn_fwd_rejects_bad_arguments(lib):
 
 def test_qkv_proj_rejects_bad_arguments(lib):
     def call(x=FAKE, W=FAKE, b=None, B=2, S=8, dm=128, H=2, qs=1.0, dt=api.LA_F32):
-        return lib.la_qkv_proj(x, W, b, FAKE, FAKE, FAKE, B, S, dm, H, qs, dt, None)
+        return lib.la_qkv_proj(x, W, b, FAKE, FAKE, FAKE, B, S, dm, H, qs, dt, None, 0, None)
     assert call(x=None) == api.LA_ERR_INVALID
     assert call(dm=129, H=2) == api.LA_ERR_INVALID        # d_model not a multiple of H
     assert call(dm=192, H=2) == api.LA_ERR_UNSUPPORTED    # D = 96
     assert call(S=-1) == api.LA_ERR_INVALID
     assert call(qs=float("nan")) == api.LA_ERR_INVALID
     assert call(b=ctypes.c_void_p(0x7f0000000001)) == api.LA_ERR_INVALID
+    assert call() == api.LA_ERR_WORKSPACE                 # fp32 transposes the weight into ws
 
 
 def test_layer_attn_checks_workspace_before_launch(lib):
@@ -103,8 +114,12 @@ def test_workspace_sizes(lib):
     assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 1, 1, 16, 16, 96, api.LA_BF16) == bad
     assert lib.la_workspace_size(9, 1, 1, 16, 16, 64, api.LA_BF16) == bad
     assert lib.la_workspace_size(api.LA_OP_LAYER_ATTN, 1, 1, 16, 32, 64, api.LA_BF16) == bad
-    # short key ranges never split
-    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_F32) == 0
+    # short key ranges never split; half precision needs nothing else
+    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_BF16) == 0
+    # fp32 holds V transposed for the TF32 tensor cores
+    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_F32) == api.fp32_vt_bytes(8, 8, 512, 64)
+    assert lib.la_workspace_size(api.LA_OP_QKV_PROJ, 8, 8, 512, 512, 64, api.LA_F32) == 3 * 512 * 512 * 4
+    assert lib.la_workspace_size(api.LA_OP_QKV_PROJ, 8, 8, 512, 512, 64, api.LA_BF16) == 0
     # the 100k-token chunked case: partials stay far below the cache itself
     n = lib.la_workspace_size(api.LA_OP_ATTN_CHUNKED, 2, 16, 4096, 100000, 64, api.LA_BF16)
     assert n != bad and n < 2 * 16 * 100000 * 64 * 2 * 4

@@ -10,6 +10,11 @@ from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
 
+
+def _id(x):
+    names = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    return names.get(x, str(x))
+
 DTYPES = [torch.float32, torch.bfloat16, torch.float16]
 
 
@@ -23,7 +28,12 @@ def _lib():
 def _gpu_attn(q, k, v, causal, kv_len=None, split=True, scale=None):
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     kl = kv_len.cuda() if kv_len is not None else None
-    ws = None if split else torch.empty(0, dtype=torch.uint8, device="cuda")
+    if split:
+        ws = None  # the binding sizes the workspace with la_workspace_size: splits allowed
+    else:       # only what an fp32 call must have (V transposed): no room for split partials
+        B, H, _, D = q.shape
+        n = api.fp32_vt_bytes(B, H, k.shape[2], D) if q.dtype == torch.float32 else 0
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     o = api.attn_fwd(qd, kd, vd, causal=causal, scale=scale, kv_len=kl, workspace=ws)
     assert api.get_last_error() == api.LA_OK
     return o
@@ -40,7 +50,7 @@ def test_c1_seed_sweep():
 SHAPES = [(2, 3, 300, 300), (1, 2, 77, 519), (1, 1, 519, 77), (2, 2, 1, 1), (1, 2, 1, 700), (3, 1, 256, 256)]
 
 
-@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("dtype", DTYPES, ids=_id)
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", SHAPES)
@@ -51,7 +61,7 @@ def test_shapes(dtype, D, causal, shape):
     assert_close(o, oracle.attn(q, k, v, causal=causal), dtype, f"{shape} D={D} causal={causal}")
 
 
-@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("dtype", DTYPES, ids=_id)
 @pytest.mark.parametrize("causal", [False, True])
 def test_key_padding(dtype, causal):
     B, H, S, D = 5, 2, 333, 64
@@ -64,7 +74,7 @@ def test_key_padding(dtype, causal):
 
 
 @pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float16, 64), (torch.float32, 64),
-                                     (torch.float32, 128)])
+                                     (torch.float32, 128)], ids=lambda p: _id(p) if not isinstance(p, int) else str(p))
 @pytest.mark.parametrize("causal", [False, True])
 def test_split_kv_equals_unsplit(dtype, D, causal):
     B, H, S_q, S_kv = 1, 2, 256, 4096 + 77

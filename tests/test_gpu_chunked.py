@@ -11,6 +11,11 @@ from layer_attn_fwd_gb300 import api, build, inputs
 pytestmark = pytest.mark.gpu
 
 
+def _id(x):
+    names = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    return names.get(x, str(x))
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     need_gpu()
@@ -31,7 +36,7 @@ def _run_chunked(q, k, v, chunk, causal=True, S_max=None):
     return torch.cat(outs, dim=2)
 
 
-@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float16, 128)])
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float16, 128)], ids=lambda p: _id(p) if not isinstance(p, int) else str(p))
 def test_chunked_small(dtype, D):
     B, H, S, C = 2, 2, 1000, 256
     q, k, v = inputs.attn_inputs(B, H, S, S, D, dtype, seed=51)

@@ -11,6 +11,11 @@ from layer_attn_fwd_gb300 import api, build, inputs
 pytestmark = pytest.mark.gpu
 
 
+def _id(x):
+    names = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    return names.get(x, str(x))
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     need_gpu()
@@ -18,7 +23,7 @@ def _lib():
     api.load()
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=_id)
 @pytest.mark.parametrize("dm,H", [(256, 4), (256, 2), (384, 6)])
 def test_qkv_proj(dtype, dm, H):
     B, S = 2, 201
@@ -46,7 +51,7 @@ def test_layer_fp32_b8_s512_d512():
     assert_close(o, oracle.layer_attn(x, W, b, 8), torch.float32, "layer")
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=_id)
 @pytest.mark.parametrize("causal", [False, True])
 def test_layer_small(dtype, causal):
     B, S, dm, H = 3, 150, 256, 2
