@@ -77,9 +77,10 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <typename T, int D_, int NQ_, int BN_, int NS_>
+template <typename T, int D_, int NQ_, int BN_, int NS_, int EMU_>
 struct Cfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, NS = NS_;
+  static constexpr int EMU = EMU_;  // of every 8 score columns, how many use the FMA-pipe exp2
   static constexpr int E = sizeof(T);
   static constexpr int CW = 128 / E;            // elements per 128-byte swizzle row
   static constexpr int NCH = D / CW;            // 128-byte chunks per row of D elements
@@ -170,11 +171,11 @@ __device__ __forceinline__ void store_out32(T* dst, const float (&v)[32]) {
   }
 }
 
-template <typename T, int D, int NQ, int BN, int NS>
-__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
+template <typename T, int D, int NQ, int BN, int NS, int EMU>
+__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using C = Cfg<T, D, NQ, BN, NS>;
+  using C = Cfg<T, D, NQ, BN, NS, EMU>;
   constexpr bool TF32 = Elem<T>::tf32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -433,14 +434,18 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
-        const float p = ex2_approx(fmaf(u2f(s[c]), sl2, -m_use));
+        // the exponentials are split between the MUFU unit and the FMA pipe
+        const float x = fmaf(u2f(s[c]), sl2, -m_use);
+        const float p = (c & 7) < EMU ? ex2_poly(x) : ex2_approx(x);
         rs += p;
         s[c] = f2u(p);
       }
       l += rs;
       store_p<T, BN>(tS, s);
-      if (grow && j > jb) {
-        // O was produced by PV of earlier tiles: rescale it to the new max.
+      // O was produced by PV of earlier tiles: rescale it to the new max.  The
+      // tensor-memory loads/stores are warp-collective, so the warp rescales
+      // together when any of its rows grew (alpha is 1 for the others).
+      if (__any_sync(0xffffffffu, grow) && j > jb) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -492,11 +497,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS>::THREADS, 1)
   }
 }
 
-template <typename T, int D, int NQ, int BN, int NS>
+template <typename T, int D, int NQ, int BN, int NS, int EMU>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                        int splits, cudaStream_t st) {
-  using C = Cfg<T, D, NQ, BN, NS>;
-  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS>;
+  using C = Cfg<T, D, NQ, BN, NS, EMU>;
+  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, EMU>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -513,6 +518,15 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 }
 
 }  // namespace
+
+#ifndef LA_EMU_D64
+#define LA_EMU_D64 3
+#endif
+#ifndef LA_EMU_D128
+#define LA_EMU_D128 1
+#endif
+constexpr int kEmuD64 = LA_EMU_D64;
+constexpr int kEmuD128 = LA_EMU_D128;
 
 // Launch shapes per (dtype, D): query rows per CTA = 128 * NQ, key tile BN,
 // stages NS; chosen so Q + NS stages of K and V fit in 227 KB of shared memory
@@ -532,16 +546,18 @@ bool attn_shape(la_dtype dt, int D, AttnShape* s) {
 
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnArgs& a, int splits, cudaStream_t st) {
+  // EMU: share of the exponentials on the FMA pipe (eighths).  At D=64 the
+  // MUFU unit alone needs twice the tensor-core time per key tile.
   switch (dt) {
     case LA_BF16:
-      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3>(tq, tk, tv, a, splits, st)
-                     : launch_one<__nv_bfloat16, 128, 2, 128, 2>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3, kEmuD64>(tq, tk, tv, a, splits, st)
+                     : launch_one<__nv_bfloat16, 128, 2, 128, 2, kEmuD128>(tq, tk, tv, a, splits, st);
     case LA_F16:
-      return D == 64 ? launch_one<__half, 64, 2, 128, 3>(tq, tk, tv, a, splits, st)
-                     : launch_one<__half, 128, 2, 128, 2>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<__half, 64, 2, 128, 3, kEmuD64>(tq, tk, tv, a, splits, st)
+                     : launch_one<__half, 128, 2, 128, 2, kEmuD128>(tq, tk, tv, a, splits, st);
     case LA_F32:
-      return D == 64 ? launch_one<float, 64, 2, 128, 2>(tq, tk, tv, a, splits, st)
-                     : launch_one<float, 128, 1, 64, 2>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<float, 64, 2, 128, 2, kEmuD64>(tq, tk, tv, a, splits, st)
+                     : launch_one<float, 128, 1, 64, 2, 0>(tq, tk, tv, a, splits, st);
   }
   return cudaErrorInvalidValue;
 }

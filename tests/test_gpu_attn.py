@@ -95,6 +95,20 @@ def test_scale_parameter():
         assert_close(o, oracle.attn(q, k, v, causal=True, scale=scale), torch.bfloat16, f"scale {scale}")
 
 
+@pytest.mark.parametrize("dtype", DTYPES, ids=_id)
+@pytest.mark.parametrize("causal", [False, True])
+def test_growing_scores_rescale(dtype, causal):
+    """Keys whose norm grows along the sequence: row maxima rise tile after
+    tile, so the running max moves (and O is rescaled) for some rows of a warp
+    and not for others."""
+    B, H, S, D = 2, 2, 700, 64
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=18)
+    k = k * (1.0 + torch.arange(S, dtype=torch.float32) / 64.0)[None, None, :, None]
+    q, k, v = (t.to(dtype) for t in (q, k, v))
+    o = _gpu_attn(q, k, v, causal, scale=0.5)
+    assert_close(o, oracle.attn(q, k, v, causal=causal, scale=0.5), dtype, "growing scores")
+
+
 def test_repeat_runs_bitwise_identical():
     q, k, v = inputs.attn_inputs(2, 4, 1000, 1000, 128, torch.bfloat16, seed=14)
     a = _gpu_attn(q, k, v, True)
