@@ -166,6 +166,37 @@ la_status la_layer_attn(const void *x, const void *Wqkv, const void *bqkv, void 
                         void *ws, size_t ws_bytes, la_stream_t st);
 
 /*
+ * la_attn_fwd without a workspace, for callers that cannot allocate device
+ * memory: a host framework whose plugin interface hands over only the input
+ * and output tensors, a service that sizes all of its device memory once at
+ * start-up and allows no allocation afterwards, or a latency-critical loop
+ * that must not call cudaMalloc (which can synchronise the device).  The
+ * pages have no counterpart; it is an addition of this library.
+ *
+ * Same arguments, meaning and result as la_attn_fwd, minus ws/ws_bytes.  Its
+ * scratch (split-KV partials; for fp32 also V transposed) is one static
+ * device array of 16 MiB inside the library, which every GPU that loads the
+ * library keeps until the process exits; the call itself allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *   - Limit: fp32 needs B*H*D*round_up(S_kv, 4)*4 bytes of it (rounded up to
+ *     256); a call beyond 16 MiB returns LA_ERR_WORKSPACE and launches
+ *     nothing.  Split partials take what is left; a call that would want more
+ *     simply splits less (bf16/fp16 never fail for lack of scratch).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose kernels can overlap
+ *     on the GPU (different streams without ordering) race on it: serialise
+ *     them.
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE or
+ * LA_ERR_CUDA.
+ */
+la_status la_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
+                              int B, int H, int S_q, int S_kv, int D, int causal, float scale,
+                              const int32_t *kv_len, la_dtype dt, la_stream_t st);
+
+/*
  * Workspace bytes an operation wants (0 if none).  op is an la_op; the
  * remaining arguments are those of the call (for LA_OP_ATTN_CHUNKED pass
  * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN and

@@ -53,6 +53,8 @@ def load(path: str | None = None):
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.la_qkv_proj.argtypes = [P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
         lib.la_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, I, P, Z, P]
+        lib.la_attn_fwd_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, I, P]
+        lib.la_attn_fwd_noalloc.restype = I
         lib.la_attn_chunked.argtypes = [P, P, P, ctypes.POINTER(la_kv_cache), P, I, I, F, P, Z, P]
         lib.la_layer_attn.argtypes = [P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
         lib.la_workspace_size.argtypes = [I, I, I, I, I, I, I]
@@ -164,6 +166,22 @@ def attn_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, workspace
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().la_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S_q, S_kv, D, int(bool(causal)), scale,
                               _ptr(kv_len), _dt(q), _ptr(workspace), nbytes, _stream(stream)), "la_attn_fwd")
+    return o
+
+
+def attn_fwd_noalloc(q, k, v, causal=False, scale=None, kv_len=None, out=None, stream=None):
+    """attn_fwd for callers that cannot allocate: the library's own static
+    16 MiB device scratch stands in for the workspace (see layerattn.h)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    if k.shape != (B, H, S_kv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B,H,S_kv,D] matching q")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    _check(load().la_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S_q, S_kv, D, int(bool(causal)),
+                                      scale, _ptr(kv_len), _dt(q), _stream(stream)), "la_attn_fwd_noalloc")
     return o
 
 

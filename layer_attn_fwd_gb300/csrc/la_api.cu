@@ -18,6 +18,12 @@
 
 __device__ uint32_t la_device_error_word;
 
+// Scratch of la_attn_fwd_noalloc(): split-KV partials (and, for fp32, V
+// transposed) for callers that cannot supply a workspace.  Every GPU that
+// loads the library holds it until the process exits.
+static constexpr size_t kNoAllocScratchBytes = 16u << 20;
+static __device__ __align__(256) uint8_t la_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace la {
 namespace {
 
@@ -469,6 +475,48 @@ size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtyp
     default:
       return bad;
   }
+}
+
+// Device address of la_noalloc_scratch on the current device.  Host code only
+// has a stand-in symbol for it, so the address is looked up once per device
+// (with that device current) and cached.
+static la_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[la::kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= la::kMaxDevices) return LA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, la_noalloc_scratch) != cudaSuccess || p == nullptr) return LA_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return LA_OK;
+}
+
+la_status la_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, int B, int H, int S_q, int S_kv,
+                              int D, int causal, float scale, const int32_t* kv_len, la_dtype dt, la_stream_t st) {
+  if ((!q || !o) && S_q != 0) return LA_ERR_INVALID;
+  if ((!k || !v) && S_kv != 0) return LA_ERR_INVALID;
+  la_status s = check_attn_args(B, H, S_q, S_kv, D, scale, dt);
+  if (s != LA_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LA_ERR_INVALID;
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return LA_ERR_INVALID;
+  if (S_q == 0) return LA_OK;
+  // fp32 needs V transposed in the scratch; beyond the array's size: refuse
+  if (vt_bytes(dt, B, H, S_kv, D) > kNoAllocScratchBytes) return LA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != LA_OK) return s;
+  if (S_kv == 0) k = v = q;  // no key is ever loaded; the maps only need a valid base
+  // Split partials go after the fp32 V^T; the split plan takes only what fits.
+  // Nothing in the scratch needs to start at zero: every byte a call reads is
+  // written earlier in the same call.
+  const KVView kv{k, v, S_kv, nullptr, 0};
+  return run_attention(q, kv, o, static_cast<long long>(H) * S_q * D, static_cast<long long>(S_q) * D, D, B, H,
+                       S_q, S_kv, D, causal, scale, kv_len, dt, scratch, kNoAllocScratchBytes,
+                       reinterpret_cast<cudaStream_t>(st));
 }
 
 la_status la_get_last_error(la_stream_t st) {
