@@ -206,6 +206,15 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     K, W = args.steps, args.warmup
 
+    if args.only:
+        # one named workload alone (for profiler captures of one kernel)
+        res = other_workloads(args, dev, stream, flush, barrier, peaks)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "workloads": res}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
     # ---- headline: the sublayer -------------------------------------------
     B, S, dm, H = HEADLINE["B"], HEADLINE["S"], HEADLINE["d_model"], HEADLINE["H"]
     D = dm // H
@@ -304,7 +313,12 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
     res = {}
     Kx = max(3, min(args.steps, 20))
 
-    def attn_case(name, B, H, S, D, dt, causal, padded=False):
+    def wanted(key):
+        return not args.only or args.only == key
+
+    def attn_case(key, name, B, H, S, D, dt, causal, padded=False):
+        if not wanted(key):
+            return
         q, k, v = (t.to(dev) for t in inputs.attn_inputs(B, H, S, S, D, dt, seed=0))
         kv = inputs.padding_kv_len(B, S) if padded else None
         kl = kv.to(dev) if kv is not None else None
@@ -320,11 +334,13 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
                      "gflop": round(fl / 1e9, 3)}
         del q, k, v, o, ws
 
-    attn_case("fp32 causal B8 H8 S2048 D64", 8, 8, 2048, 64, torch.float32, True)
-    attn_case("fp32 causal B8 H8 S2048 D64, last 25% keys padded for half the batch", 8, 8, 2048, 64,
-              torch.float32, True, padded=True)
-    attn_case("bf16 causal B4 H16 S4096 D128", 4, 16, 4096, 128, torch.bfloat16, True)
-    attn_case("fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False)
+    attn_case("fp32-causal-2048", "fp32 causal B8 H8 S2048 D64", 8, 8, 2048, 64, torch.float32, True)
+    attn_case("fp32-causal-2048-padded", "fp32 causal B8 H8 S2048 D64, last 25% keys padded for half the batch",
+              8, 8, 2048, 64, torch.float32, True, padded=True)
+    attn_case("bf16-causal-4096", "bf16 causal B4 H16 S4096 D128", 4, 16, 4096, 128, torch.bfloat16, True)
+    attn_case("fp32-small", "fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False)
+    if not wanted("chunked-100k"):
+        return res
 
     # chunked 100k-token mode: 25 windows of 4096 (the last 1696) per step
     B, H, S, D, C = 2, 16, 100000, 64, 4096
@@ -345,7 +361,8 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
             api.attn_chunked(qs[i], ks[i], vs[i], cache, out=outs[i], workspace=ws, stream=stream)
 
     torch.cuda.reset_peak_memory_stats(dev)
-    ms = _time_steps(chunked_step, 3, 1, flush, stream, barrier) / 3
+    kc = 3 if not args.only else max(1, min(args.steps, 3))
+    ms = _time_steps(chunked_step, kc, 1, flush, stream, barrier) / kc
     fl = flops.attn_flops(B, H, S, S, D, True)
     tf = fl / (ms * 1e-3) / 1e12
     res["chunked bf16 causal B2 H16 S100000 D64, windows of 4096"] = {
@@ -425,6 +442,9 @@ def main():
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--only", choices=["fp32-causal-2048", "fp32-causal-2048-padded", "bf16-causal-4096",
+                                       "fp32-small", "chunked-100k"],
+                    help="time one named attention workload alone and print its figures (no contract line)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")

@@ -419,9 +419,17 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= lim) s[c] = f2u(-INFINITY);
       }
-      float mx = u2f(s[0]);
+      // row max: 8 independent partial maxima, then a tree (no 128-long
+      // dependency chain)
+      float mxa[8];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, u2f(s[c]));
+      for (int k = 0; k < 8; ++k) mxa[k] = u2f(s[k]);
+#pragma unroll
+      for (int c = 8; c < BN; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(mxa[k], u2f(s[c + k]));
+      const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                             fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool grow = m_new > m_run + 8.0f;
       float alpha = 1.f;
@@ -431,16 +439,18 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
         m_run = m_new;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float rs = 0.f;
+      float rsa[8];  // row sum: 8 independent partial sums
+#pragma unroll
+      for (int k = 0; k < 8; ++k) rsa[k] = 0.f;
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
-        // the exponentials are split between the MUFU unit and the FMA pipe
+        // the exponentials may be split between the MUFU unit and the FMA pipe
         const float x = fmaf(u2f(s[c]), sl2, -m_use);
         const float p = (c & 7) < EMU ? ex2_poly(x) : ex2_approx(x);
-        rs += p;
+        rsa[c & 7] += p;
         s[c] = f2u(p);
       }
-      l += rs;
+      l += ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])) + ((rsa[4] + rsa[5]) + (rsa[6] + rsa[7]));
       store_p<T, BN>(tS, s);
       // O was produced by PV of earlier tiles: rescale it to the new max.  The
       // tensor-memory loads/stores are warp-collective, so the warp rescales
@@ -520,10 +530,10 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 }  // namespace
 
 #ifndef LA_EMU_D64
-#define LA_EMU_D64 3
+#define LA_EMU_D64 0
 #endif
 #ifndef LA_EMU_D128
-#define LA_EMU_D128 1
+#define LA_EMU_D128 0
 #endif
 constexpr int kEmuD64 = LA_EMU_D64;
 constexpr int kEmuD128 = LA_EMU_D128;
@@ -546,8 +556,9 @@ bool attn_shape(la_dtype dt, int D, AttnShape* s) {
 
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnArgs& a, int splits, cudaStream_t st) {
-  // EMU: share of the exponentials on the FMA pipe (eighths).  At D=64 the
-  // MUFU unit alone needs twice the tensor-core time per key tile.
+  // EMU: share of the exponentials on the FMA pipe (eighths).  Measured on
+  // GB300: every share above 0 was slower (the MUFU unit is not the limit:
+  // ncu shows the XU pipe about 20% busy), so it is 0.
   switch (dt) {
     case LA_BF16:
       return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3, kEmuD64>(tq, tk, tv, a, splits, st)

@@ -72,7 +72,8 @@ struct PCfg {
   static constexpr int OFF_BAR = OFF_B + NSP * B_STAGE;
   static constexpr int NBAR = 2 * NSP + 2;     // full[NSP], empty[NSP], acc_full, mma_done
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_BIAS = OFF_MISC + 16;  // the tile's BNP bias values (fp32)
+  static constexpr int SMEM_BYTES = OFF_BIAS + BNP * 4 + 1024;
   static constexpr int TMEM_COLS = BNP;
   static constexpr int ROWS_PER_KSTEP = 32 / E;  // K rows consumed by one MMA
   static constexpr int THREADS = 192;
@@ -206,7 +207,14 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   } else {
-    // epilogue: thread owns output row m; 32 columns at a time
+    // epilogue: thread owns output row m; 32 columns at a time.  First stage
+    // the tile's bias slice in shared memory while the main loop runs.
+    float* sbias = reinterpret_cast<float*>(smem + C::OFF_BIAS);
+    for (int i = threadIdx.x; i < BNP; i += 128) {
+      const int n = tile_n * BNP + i;
+      sbias[i] = (a.bias != nullptr && n < a.N) ? PElem<T>::load(a.bias, n) : 0.f;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps only
     const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, ab, SITE_PROJ_ACC));
     if (ok) {
       tc_fence_after();
@@ -229,9 +237,7 @@ __global__ void __launch_bounds__(192, 1)
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          float y = __uint_as_float(acc[c]);
-          if (a.bias != nullptr) y += PElem<T>::load(a.bias, n0 + c);
-          v[c] = y * mul;
+          v[c] = (__uint_as_float(acc[c]) + sbias[c0 + c]) * mul;
         }
         if (m < a.M) {
           if (which == 2 && a.v_transposed) {

@@ -30,3 +30,12 @@ def assert_close(got, want, dtype, what=""):
             f"{what}: {int(bad.sum())} of {bad.size} elements outside atol={atol} rtol={rtol}; "
             f"max abs err {err.max():.3g}; worst at {idx}: got {g[idx]:.6g} want {want[idx]:.6g}")
     return float(err.max())
+
+
+def tf32_round(t):
+    """fp32 values rounded to TF32 (10 fraction bits, nearest, ties to even):
+    the operands the TF32 tensor-core products see after the rounding copy."""
+    b = t.detach().float().contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+    b = (b + 0x0FFF + ((b >> 13) & 1)) & 0xFFFFE000
+    b = torch.where(b >= 2 ** 31, b - 2 ** 32, b).to(torch.int32)
+    return b.view(torch.float32).reshape(t.shape)

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, need_gpu
+from gpu_util import assert_close, need_gpu, tf32_round
 from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +30,11 @@ def test_qkv_proj(dtype, dm, H):
     x, W, b = inputs.layer_inputs(B, S, dm, dtype, seed=41, bias="normal")
     q, k, v = api.qkv_proj(x.cuda(), W.cuda(), b.cuda(), H, q_scale=0.5)
     assert api.get_last_error() == api.LA_OK
-    wq, wk, wv = oracle.qkv_proj(x, W, b, H, q_scale=0.5)
+    # fp32 runs on TF32 tensor cores: a K-long dot product of TF32-rounded
+    # operands can miss 1e-3 at K = 384 on its own, so fp32 is checked on the
+    # operands the tensor cores see (the sublayer tests check fp32 end to end)
+    xr, Wr = (x, W) if dtype != torch.float32 else (tf32_round(x), tf32_round(W))
+    wq, wk, wv = oracle.qkv_proj(xr, Wr, b, H, q_scale=0.5)
     for got, want, n in ((q, wq, "q"), (k, wk, "k"), (v, wv, "v")):
         assert_close(got, want, dtype, n)
 
