@@ -132,12 +132,9 @@ template <typename T, int BN>
 __device__ __forceinline__ void store_p(uint32_t taddr, uint32_t (&s)[BN]) {
   if constexpr (Elem<T>::tf32) {
 #pragma unroll
-    for (int h = 0; h < BN / 64; ++h) {
-      uint32_t a[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) a[c] = f32_to_tf32(u2f(s[64 * h + c]));
-      tmem_st_x64(taddr + 64 * h, a);
-    }
+    for (int c = 0; c < BN; ++c) s[c] = f32_to_tf32(u2f(s[c]));
+    tmem_st_x64_at<0>(taddr, s);
+    if constexpr (BN == 128) tmem_st_x64_at<64>(taddr + 64, s);
   } else {
     uint32_t pk[BN / 2];
 #pragma unroll
@@ -306,43 +303,27 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     if (lane == 0 && je_all > jb) {
       const uint32_t idesc_qk = idesc_make(Elem<T>::ab, kTileM, BN, false, false);
       const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, !C::VT);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-      const uint32_t sK = smem_u32(smem + C::OFF_K);
-      const uint32_t sV = smem_u32(smem + C::OFF_V);
-      // S_t = Q_t K_j^T: both operands K-major; one MMA per 32 bytes of a row.
-      auto issue_s = [&](int t, int j) {
-        const int s = (j - jb) % NS;
-        const uint32_t d = tmem + t * C::TILE_COLS;
-#pragma unroll
-        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-          const uint32_t o = (kk & 3) * 32;  // byte offset inside the 128-byte row
-          const uint64_t ad = sdesc_sw128(sQ + t * C::Q_TILE + (kk >> 2) * C::Q_CHUNK + o, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + s * C::KV_TILE + (kk >> 2) * C::KV_CHUNK + o, 16, 1024);
-          mma_ss<TF32>(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t += P_t V_j: P from tensor memory; V MN-major (rows = keys), or for
-      // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step).
-      auto issue_pv = [&](int t, int j) {
-        const int s = (j - jb) % NS;
-        const uint32_t d = tmem + t * C::TILE_COLS + BN;
-        const uint32_t p = tmem + t * C::TILE_COLS;
-#pragma unroll
-        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-          uint64_t bd;
-          if constexpr (C::VT)
-            bd = sdesc_sw128(sV + s * C::KV_TILE + (kk >> 2) * C::VT_CHUNK + (kk & 3) * 32, 16, 1024);
-          else
-            bd = sdesc_sw128(sV + s * C::KV_TILE + kk * C::PV_ROWS * 128, C::KV_CHUNK, 1024);
-          mma_ts<TF32>(d, p + kk * 8, bd, idesc_pv, (j > jb || kk > 0) ? 1u : 0u);
-        }
-      };
+      // Shared-memory descriptors of the tile bases; the start address field
+      // holds address >> 4 and every address here stays below 2^18, so a byte
+      // offset is added to a descriptor as (offset >> 4).
+      const uint64_t dQ = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+      const uint64_t dV = C::VT ? sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024)
+                                : sdesc_sw128(smem_u32(smem + C::OFF_V), C::KV_CHUNK, 1024);
       bool ok = mbar_wait(q_full, 0, ab, SITE_Q_FULL) && mbar_wait(&k_full[0], 0, ab, SITE_K_FULL);
       if (ok) {
         tc_fence_after();
+#pragma unroll
         for (int t = 0; t < NQ; ++t) {
           if (je[t] > jb) {
-            issue_s(t, jb);
+            // S_t = Q_t K^T: both operands K-major; one MMA per 32 bytes of a row
+            const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+              const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
+              const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
+              mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, dK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
+            }
             mma_commit(&s_full[t]);
           }
         }
@@ -351,23 +332,39 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       for (int j = jb; ok && j < je_all; ++j) {
         const int i = j - jb, s = i % NS, r = i / NS;
         const int sn = (i + 1) % NS, rn = (i + 1) / NS;
+        const uint64_t bV = dV + ((s * C::KV_TILE) >> 4);
+        const uint64_t bK = dK + ((sn * C::KV_TILE) >> 4);
         bool v_ready = false, k_next = false;
-        for (int t = 0; t < NQ && ok; ++t) {
-          if (j >= je[t]) continue;
-          if (!mbar_wait(&p_full[t], i & 1, ab, SITE_P_FULL)) { ok = false; break; }
-          if (!v_ready) {
-            if (!mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL)) { ok = false; break; }
-            v_ready = true;
-          }
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (!ok || j >= je[t]) continue;
+          ok = mbar_wait(&p_full[t], i & 1, ab, SITE_P_FULL);
+          if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
+          if (!ok) continue;
           tc_fence_after();
-          issue_pv(t, j);
+          // O_t += P_t V: P from tensor memory; V MN-major (rows = keys), or for
+          // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step)
+          const uint32_t d_o = tmem + t * C::TILE_COLS + BN;
+          const uint32_t p_t = tmem + t * C::TILE_COLS;
+#pragma unroll
+          for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+            const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
+                                       : (kk * C::PV_ROWS * 128) >> 4;
+            mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > jb || kk > 0) ? 1u : 0u);
+          }
           if (j + 1 < je[t]) {
             if (!k_next) {
-              if (!mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL)) { ok = false; break; }
+              ok = k_next = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+              if (!ok) continue;
               tc_fence_after();
-              k_next = true;
             }
-            issue_s(t, j + 1);
+            const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+              const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
+              const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
+              mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
+            }
             mma_commit(&s_full[t]);
           } else {
             mma_commit(&o_full[t]);
@@ -402,8 +399,12 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     const float sl2 = a.sl2;
     float m_run = -INFINITY;  // running max, in log2 units of the scaled scores
     float l = 0.f;            // running sum of P
+    int je_t = jb;  // this tile's key-tile end, kept in a register
+#pragma unroll
+    for (int u = 0; u < NQ; ++u)
+      if (u == t) je_t = je[u];
     bool ok = true;
-    for (int j = jb; j < je[t]; ++j) {
+    for (int j = jb; j < je_t; ++j) {
       const int i = j - jb;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], i & 1, ab, SITE_S_FULL));
       if (!ok) break;
@@ -443,14 +444,26 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) rsa[k] = 0.f;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
+      for (int c = 0; c < BN; c += 2) {
+        // exponent arguments and partial sums two columns per instruction
+        float x0, x1;
+        fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), sl2, sl2, -m_use, -m_use);
         // the exponentials may be split between the MUFU unit and the FMA pipe
-        const float x = fmaf(u2f(s[c]), sl2, -m_use);
-        const float p = (c & 7) < EMU ? ex2_poly(x) : ex2_approx(x);
-        rsa[c & 7] += p;
-        s[c] = f2u(p);
+        const float p0 = (c & 7) < EMU ? ex2_poly(x0) : ex2_approx(x0);
+        const float p1 = ((c + 1) & 7) < EMU ? ex2_poly(x1) : ex2_approx(x1);
+        float& r0 = rsa[c & 7];
+        float& r1 = rsa[(c & 7) + 1];
+        add2(r0, r1, r0, r1, p0, p1);
+        s[c] = f2u(p0);
+        s[c + 1] = f2u(p1);
       }
-      l += ((rsa[0] + rsa[1]) + (rsa[2] + rsa[3])) + ((rsa[4] + rsa[5]) + (rsa[6] + rsa[7]));
+      {
+        float a0, a1, b0, b1;
+        add2(a0, a1, rsa[0], rsa[1], rsa[2], rsa[3]);
+        add2(b0, b1, rsa[4], rsa[5], rsa[6], rsa[7]);
+        add2(a0, a1, a0, a1, b0, b1);
+        l += a0 + a1;
+      }
       store_p<T, BN>(tS, s);
       // O was produced by PV of earlier tiles: rescale it to the new max.  The
       // tensor-memory loads/stores are warp-collective, so the warp rescales
@@ -470,7 +483,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    const bool has_o = je[t] > jb;
+    const bool has_o = je_t > jb;
     if (ok && has_o) {
       ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, ab, SITE_O_FULL));
       if (ok) tc_fence_after();

@@ -176,21 +176,22 @@ __host__ __device__ constexpr uint32_t idesc_make(uint32_t ab, int M, int N, boo
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc)
+// D(tmem) (+)= A(smem desc) * B(smem desc).  No "memory" clobber: the MMA
+// reads shared memory through the async proxy, ordered by the mbarrier waits
+// and tcgen05 fences around it, and volatile asm statements keep their order,
+// so the compiler may keep everything else in registers across the issue.
 template <bool TF32>
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if constexpr (TF32) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
   } else {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
   }
 }
 // D(tmem) (+)= A(tmem) * B(smem desc)
@@ -201,14 +202,12 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
   } else {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
   }
 }
 // Arrive once on the mbarrier when every MMA this thread issued so far is done.
@@ -274,6 +273,15 @@ __device__ __forceinline__ void tmem_st_x64(uint32_t taddr, const uint32_t (&v)[
                : "memory");
 }
 
+// Store columns [OFF, OFF + 64) of a register row (no copy of the row).
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_st_x64_at(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(OFF + 64 <= N, "row slice");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
+               :: "r"(taddr), "r"(v[OFF + 0]), "r"(v[OFF + 1]), "r"(v[OFF + 2]), "r"(v[OFF + 3]), "r"(v[OFF + 4]), "r"(v[OFF + 5]), "r"(v[OFF + 6]), "r"(v[OFF + 7]), "r"(v[OFF + 8]), "r"(v[OFF + 9]), "r"(v[OFF + 10]), "r"(v[OFF + 11]), "r"(v[OFF + 12]), "r"(v[OFF + 13]), "r"(v[OFF + 14]), "r"(v[OFF + 15]), "r"(v[OFF + 16]), "r"(v[OFF + 17]), "r"(v[OFF + 18]), "r"(v[OFF + 19]), "r"(v[OFF + 20]), "r"(v[OFF + 21]), "r"(v[OFF + 22]), "r"(v[OFF + 23]), "r"(v[OFF + 24]), "r"(v[OFF + 25]), "r"(v[OFF + 26]), "r"(v[OFF + 27]), "r"(v[OFF + 28]), "r"(v[OFF + 29]), "r"(v[OFF + 30]), "r"(v[OFF + 31]), "r"(v[OFF + 32]), "r"(v[OFF + 33]), "r"(v[OFF + 34]), "r"(v[OFF + 35]), "r"(v[OFF + 36]), "r"(v[OFF + 37]), "r"(v[OFF + 38]), "r"(v[OFF + 39]), "r"(v[OFF + 40]), "r"(v[OFF + 41]), "r"(v[OFF + 42]), "r"(v[OFF + 43]), "r"(v[OFF + 44]), "r"(v[OFF + 45]), "r"(v[OFF + 46]), "r"(v[OFF + 47]), "r"(v[OFF + 48]), "r"(v[OFF + 49]), "r"(v[OFF + 50]), "r"(v[OFF + 51]), "r"(v[OFF + 52]), "r"(v[OFF + 53]), "r"(v[OFF + 54]), "r"(v[OFF + 55]), "r"(v[OFF + 56]), "r"(v[OFF + 57]), "r"(v[OFF + 58]), "r"(v[OFF + 59]), "r"(v[OFF + 60]), "r"(v[OFF + 61]), "r"(v[OFF + 62]), "r"(v[OFF + 63])
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // numeric helpers
 // ---------------------------------------------------------------------------
@@ -299,6 +307,24 @@ __device__ __forceinline__ float ex2_poly(float x) {
   p = fmaf(p, f, 0.99992806f);
   const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
   return x < -125.0f ? 0.0f : r;
+}
+
+// Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction for two
+// lanes' worth of work.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // fp32 -> tf32 (round to nearest, ties away), kept in a 32-bit container
