@@ -219,7 +219,8 @@ la_status la_get_last_error(la_stream_t st);
  * bit 8+i wait site i gave up (0 Q loaded, 1 K loaded, 2 V loaded, 3 K slot
  * free, 4 V slot free, 5 scores ready, 6 probabilities ready, 7 output ready,
  * 8 projection stage loaded, 9 projection stage free, 10 projection
- * accumulator ready).  For diagnostics; 0 when all was well.
+ * accumulator ready, 11 projection accumulator free).  For diagnostics; 0
+ * when all was well.
  */
 uint32_t la_last_error_detail(void);
 

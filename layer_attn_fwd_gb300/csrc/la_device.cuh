@@ -62,7 +62,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait sites, recorded as bit (8 + site) of the error word when a wait runs out.
 enum WaitSite : uint32_t {
   SITE_Q_FULL = 0, SITE_K_FULL, SITE_V_FULL, SITE_K_EMPTY, SITE_V_EMPTY, SITE_S_FULL, SITE_P_FULL,
-  SITE_O_FULL, SITE_PROJ_FULL, SITE_PROJ_EMPTY, SITE_PROJ_ACC
+  SITE_O_FULL, SITE_PROJ_FULL, SITE_PROJ_EMPTY, SITE_PROJ_ACC, SITE_PROJ_ACC_FREE
 };
 
 // Wait until the phase with the given parity has completed.  Returns false

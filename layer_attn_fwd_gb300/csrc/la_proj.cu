@@ -3,15 +3,17 @@
 //
 //   y[M, 3d] = x[M, d] . Wqkv[d, 3d] + bqkv      (M = B*S rows)
 //
-// One CTA computes a 128 x BNP tile of y with tcgen05.mma (accumulator in
-// tensor memory), then its epilogue adds the bias, scales the Q block and
-// scatters the tile straight into the head-major q, k, v [B, H, S, D] outputs,
-// so the split into heads costs no extra pass.
+// A persistent kernel, one CTA per SM, walks 128 x BNP tiles of y.  Each tile
+// is accumulated in tensor memory by tcgen05.mma; the accumulator is double
+// buffered, so the epilogue of one tile (bias, Q scale, split into heads)
+// runs while the next tile's products are issued.  The epilogue scatters the
+// tile straight into the head-major q, k, v [B, H, S, D] outputs, so the
+// split into heads costs no extra pass.
 //
-//   warp 4        TMA: x tile (K-major) and Wqkv tile (rows = K, columns = N,
-//                 i.e. the B operand is MN-major) through an NSP-stage ring.
-//                 TF32 products take K-major operands only, so for fp32 the
-//                 weight is read from its transpose Wqkv^T [3d, d].
+//   warp 4        TMA: x tile (K-major) and weight tile through an NSP-stage
+//                 ring.  bf16/fp16 read Wqkv itself (rows = K, columns = N:
+//                 an MN-major operand).  TF32 products take K-major operands
+//                 only, so fp32 reads Wqkv^T [3d, d], transposed beforehand.
 //   warp 5        one thread issues the MMAs; commits free the stages.
 //   warps 0..3    epilogue, thread r owns row r of the tile.
 #include <cuda_bf16.h>
@@ -64,69 +66,74 @@ struct PCfg {
   static constexpr int E = sizeof(T);
   static constexpr int CW = 128 / E;           // elements per 128-byte row = K per stage
   static constexpr int A_STAGE = kTileM * 128; // x tile: 128 rows x 128 bytes
-  static constexpr bool WT = (E == 4);         // weight tile from Wqkv^T (K-major)
-  static constexpr int B_CHUNK = WT ? BNP * 128 : CW * 128;  // MN-major: CW weight rows x 128 bytes
+  static constexpr bool KMAJ = (E == 4);       // fp32: weight tile from Wqkv^T (K-major)
+  static constexpr int B_CHUNK = KMAJ ? BNP * 128 : CW * 128;  // MN-major: CW weight rows x 128 bytes
   static constexpr int B_STAGE = BNP * CW * E;
+  static constexpr int STG_BYTES = 32 * 128;   // one epilogue warp's 32 rows x 128 bytes
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = NSP * A_STAGE;
-  static constexpr int OFF_BAR = OFF_B + NSP * B_STAGE;
-  static constexpr int NBAR = 2 * NSP + 2;     // full[NSP], empty[NSP], acc_full, mma_done
+  static constexpr int OFF_STG = OFF_B + NSP * B_STAGE;
+  static constexpr int OFF_BIAS = OFF_STG + 4 * STG_BYTES;  // each epilogue warp's bias slice (fp32)
+  static constexpr int OFF_BAR = OFF_BIAS + 4 * BNP * 4;
+  // full[NSP], empty[NSP], acc_full[2], acc_empty[2], mma_done
+  static constexpr int NBAR = 2 * NSP + 5;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_BIAS = OFF_MISC + 16;  // the tile's BNP bias values (fp32)
-  static constexpr int SMEM_BYTES = OFF_BIAS + BNP * 4 + 1024;
-  static constexpr int TMEM_COLS = BNP;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = 2 * BNP <= 256 ? 256 : 512;  // two accumulators (power of two)
   static constexpr int ROWS_PER_KSTEP = 32 / E;  // K rows consumed by one MMA
   static constexpr int THREADS = 192;
   static constexpr int WARP_TMA = 4, WARP_MMA = 5;
-  static_assert(BNP % CW == 0 && BNP >= 32 && BNP <= 256, "tile width");
+  static_assert(BNP % CW == 0 && BNP >= 32 && BNP <= 256 && BNP % 16 == 0, "tile width");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+// Packs CW values of one row (128 bytes) into eight 16-byte units.
 template <typename T>
-__device__ __forceinline__ void store32(T* dst, const float (&v)[32]) {
+__device__ __forceinline__ uint4 pack_unit(const float* v, int u) {
   if constexpr (PElem<T>::tf32) {
-    float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    return make_uint4(__float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]), __float_as_uint(v[4 * u + 2]),
+                      __float_as_uint(v[4 * u + 3]));
   } else {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 w;
-      w.x = PElem<T>::pack2(v[8 * i + 0], v[8 * i + 1]);
-      w.y = PElem<T>::pack2(v[8 * i + 2], v[8 * i + 3]);
-      w.z = PElem<T>::pack2(v[8 * i + 4], v[8 * i + 5]);
-      w.w = PElem<T>::pack2(v[8 * i + 6], v[8 * i + 7]);
-      d4[i] = w;
-    }
+    uint4 w;
+    w.x = PElem<T>::pack2(v[8 * u + 0], v[8 * u + 1]);
+    w.y = PElem<T>::pack2(v[8 * u + 2], v[8 * u + 3]);
+    w.z = PElem<T>::pack2(v[8 * u + 4], v[8 * u + 5]);
+    w.w = PElem<T>::pack2(v[8 * u + 6], v[8 * u + 7]);
+    return w;
   }
 }
 
 template <typename T, int BNP, int NSP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const ProjArgs a) {
   using C = PCfg<T, BNP, NSP>;
   constexpr bool TF32 = PElem<T>::tf32;
+  constexpr int CW = C::CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NSP;
   uint64_t* acc_full = empty + NSP;
-  uint64_t* mma_done = acc_full + 1;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_n = blockIdx.x, tile_m = blockIdx.y;
-  const int n_k = (a.K + C::CW - 1) / C::CW;
+  const int n_tn = (a.N + BNP - 1) / BNP;
+  const int n_tiles = n_tn * ((a.M + kTileM - 1) / kTileM);
+  const int n_k = a.K / CW;  // K = d_model, a multiple of 64
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSP; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrive per epilogue warp
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -151,19 +158,24 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tm_w);
       const uint64_t pol_x = policy_evict_first();
       const uint64_t pol_w = policy_evict_last();
-      for (int kt = 0; kt < n_k; ++kt) {
-        const int s = kt % NSP, r = kt / NSP;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, ab, SITE_PROJ_EMPTY)) break;
-        mbar_arrive_expect_tx(&full[s], C::A_STAGE + C::B_STAGE);
-        tma_load_2d(&tm_x, &full[s], smem + C::OFF_A + s * C::A_STAGE, kt * C::CW, tile_m * kTileM, pol_x);
-        if constexpr (C::WT) {
-          tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE, kt * C::CW, tile_n * BNP, pol_w);
-        } else {
-          for (int c = 0; c < BNP / C::CW; ++c)
-            tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE + c * C::B_CHUNK,
-                        tile_n * BNP + c * C::CW, kt * C::CW, pol_w);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        const int tm = t / n_tn, tn = t - tm * n_tn;
+        for (int kt = 0; kt < n_k; ++kt, ++it) {
+          const int s = it % NSP, r = it / NSP;
+          if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, ab, SITE_PROJ_EMPTY)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], C::A_STAGE + C::B_STAGE);
+          tma_load_2d(&tm_x, &full[s], smem + C::OFF_A + s * C::A_STAGE, kt * CW, tm * kTileM, pol_x);
+          if constexpr (C::KMAJ) {
+            tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE, kt * CW, tn * BNP, pol_w);
+          } else {
+            for (int c = 0; c < BNP / CW; ++c)
+              tma_load_2d(&tm_w, &full[s], smem + C::OFF_B + s * C::B_STAGE + c * C::B_CHUNK, tn * BNP + c * CW,
+                          kt * CW, pol_w);
+          }
+          last[s] = r;
         }
-        last[s] = r;
       }
     }
     __syncwarp();
@@ -175,25 +187,32 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == C::WARP_MMA) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_make(PElem<T>::ab, kTileM, BNP, false, !C::WT);
+      const uint32_t idesc = idesc_make(PElem<T>::ab, kTileM, BNP, false, !C::KMAJ);
       const uint32_t sA = smem_u32(smem + C::OFF_A);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
+      int it = 0, lt = 0;
       bool ok = true;
-      for (int kt = 0; kt < n_k; ++kt) {
-        const int s = kt % NSP, r = kt / NSP;
-        if (!mbar_wait(&full[s], r & 1, ab, SITE_PROJ_FULL)) { ok = false; break; }
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++lt) {
+        const int accb = lt & 1, use = lt >> 1;
+        if (use > 0 && !mbar_wait(&acc_empty[accb], (use - 1) & 1, ab, SITE_PROJ_ACC_FREE)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t d = tmem + accb * BNP;
+        for (int kt = 0; kt < n_k; ++kt, ++it) {
+          const int s = it % NSP, r = it / NSP;
+          if (!mbar_wait(&full[s], r & 1, ab, SITE_PROJ_FULL)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = sdesc_sw128(sA + s * C::A_STAGE + kk * 32, 16, 1024);
-          const uint64_t bd =
-              C::WT ? sdesc_sw128(sB + s * C::B_STAGE + kk * 32, 16, 1024)
-                    : sdesc_sw128(sB + s * C::B_STAGE + kk * C::ROWS_PER_KSTEP * 128, C::B_CHUNK, 1024);
-          mma_ss<TF32>(tmem, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(sA + s * C::A_STAGE + kk * 32, 16, 1024);
+            const uint64_t bd =
+                C::KMAJ ? sdesc_sw128(sB + s * C::B_STAGE + kk * 32, 16, 1024)
+                      : sdesc_sw128(sB + s * C::B_STAGE + kk * C::ROWS_PER_KSTEP * 128, C::B_CHUNK, 1024);
+            mma_ss<TF32>(d, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
         }
-        mma_commit(&empty[s]);
+        if (ok) mma_commit(&acc_full[accb]);
       }
-      if (ok) mma_commit(acc_full);
     }
     __syncwarp();
     __syncthreads();
@@ -207,51 +226,87 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   } else {
-    // epilogue: thread owns output row m; 32 columns at a time.  First stage
-    // the tile's bias slice in shared memory while the main loop runs.
-    float* sbias = reinterpret_cast<float*>(smem + C::OFF_BIAS);
-    for (int i = threadIdx.x; i < BNP; i += 128) {
-      const int n = tile_n * BNP + i;
-      sbias[i] = (a.bias != nullptr && n < a.N) ? PElem<T>::load(a.bias, n) : 0.f;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps only
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, ab, SITE_PROJ_ACC));
-    if (ok) {
+    // epilogue: thread owns row warp*32 + lane of the tile.  Per 128-byte
+    // column chunk (CW columns, inside one head of one of q/k/v): TMEM ->
+    // registers, + bias, x q_scale; then the warp's 32 rows go through a
+    // swizzled 4 KB shared buffer so that every global store instruction
+    // writes whole 128-byte row segments (four rows per instruction).
+    // V^T for the fp32 sublayer is stored directly: there lanes hold
+    // consecutive positions of one V^T row, which is already coalesced.
+    float* sbias = reinterpret_cast<float*>(smem + C::OFF_BIAS) + warp * BNP;
+    uint8_t* stg = smem + C::OFF_STG + warp * C::STG_BYTES;
+    const int d_model = a.K;
+    const int sub = lane >> 3, unit = lane & 7;  // row-in-4 and 16-byte unit this lane stores
+    int lt = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
+      const int tm = t / n_tn, tn = t - tm * n_tn;
+      const int accb = lt & 1, use = lt >> 1;
+      // the tile's bias slice, one private copy per warp (no barrier beyond the warp)
+      __syncwarp();
+      for (int i = lane; i < BNP; i += 32) {
+        const int n = tn * BNP + i;
+        sbias[i] = (a.bias != nullptr && n < a.N) ? PElem<T>::load(a.bias, n) : 0.f;
+      }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[accb], use & 1, ab, SITE_PROJ_ACC))) break;
       tc_fence_after();
-      const int m = tile_m * kTileM + warp * 32 + lane;
-      const int d_model = a.K;
+      const int m = tm * kTileM + warp * 32 + lane;
       const int bidx = m / a.S;
       const int srow = m - bidx * a.S;
-      const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      // element offset of this thread's row inside one [B, H, S, D] output, head 0
+      const long long row_off = (static_cast<long long>(bidx) * a.H * a.S + srow) * a.D;
+      const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16) + accb * BNP;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BNP; c0 += 32) {
-        const int n0 = tile_n * BNP + c0;
+      for (int c0 = 0; c0 < BNP; c0 += CW) {
+        const int n0 = tn * BNP + c0;
         if (n0 >= a.N) break;  // warp-uniform
-        uint32_t acc[32];
-        tmem_ld_x32(trow + c0, acc);
+        float v[CW];
+#pragma unroll
+        for (int h = 0; h < CW / 32; ++h) {
+          uint32_t acc[32];
+          tmem_ld_x32(trow + c0 + 32 * h, acc);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[32 * h + c] = __uint_as_float(acc[c]);
+        }
         const int which = n0 / d_model;
         const int hd = n0 - which * d_model;
         const int hh = hd / a.D;
         const int dd = hd - hh * a.D;
         const float mul = which == 0 ? a.q_scale : 1.f;
-        float v[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          v[c] = (__uint_as_float(acc[c]) + sbias[c0 + c]) * mul;
-        }
-        if (m < a.M) {
-          if (which == 2 && a.v_transposed) {
-            // V^T [B, H, D, S_pad]: lanes hold consecutive rows, so each store is coalesced
-            T* out = reinterpret_cast<T*>(a.v) + ((static_cast<long long>(bidx) * a.H + hh) * a.D + dd) * a.S_pad + srow;
+        for (int c = 0; c < CW; ++c) v[c] = (v[c] + sbias[c0 + c]) * mul;
+        if (which == 2 && a.v_transposed) {
+          // V^T [B, H, D, S_pad]: lanes hold consecutive rows, so each store is coalesced
+          if (m < a.M) {
+            T* out =
+                reinterpret_cast<T*>(a.v) + ((static_cast<long long>(bidx) * a.H + hh) * a.D + dd) * a.S_pad + srow;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) out[c * a.S_pad] = static_cast<T>(v[c]);
-          } else {
-            T* out = reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v));
-            store32<T>(out + ((static_cast<long long>(bidx) * a.H + hh) * a.S + srow) * a.D + dd, v);
+            for (int c = 0; c < CW; ++c) out[c * a.S_pad] = static_cast<T>(v[c]);
+          }
+        } else {
+          // row `lane` of the buffer, 16-byte unit u at u ^ lane%8 (conflict-free both ways)
+          __syncwarp();  // the previous chunk's reads of the buffer are done
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((u ^ (lane & 7)) << 4)) = pack_unit<T>(v, u);
+          __syncwarp();
+          T* out = reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v));
+          const long long head_off = static_cast<long long>(hh) * a.S * a.D + dd;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + sub;  // the row this lane stores now
+            const long long ro = __shfl_sync(0xffffffffu, row_off, r);
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((unit ^ (r & 7)) << 4));
+            if (tm * kTileM + warp * 32 + r < a.M)
+              *reinterpret_cast<uint4*>(out + ro + head_off + unit * (16 / C::E)) = w;
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[accb]);
     }
+    __syncwarp();
     __syncthreads();
   }
 }
@@ -270,7 +325,12 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArg
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid((a.N + BNP - 1) / BNP, (a.M + kTileM - 1) / kTileM);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long tiles =
+      static_cast<long long>((a.N + BNP - 1) / BNP) * ((a.M + kTileM - 1) / kTileM);
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tx, tw, a);
   return cudaGetLastError();
 }
@@ -280,7 +340,7 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArg
 bool proj_shape(la_dtype dt, ProjShape* s) {
   if (dt != LA_F32 && dt != LA_BF16 && dt != LA_F16) return false;
   const int e = dt == LA_F32 ? 4 : 2;
-  s->block_n = 256;
+  s->block_n = dt == LA_F32 ? 192 : 256;
   s->box_cols = 128 / e;
   s->box_k_rows = 128 / e;
   s->w_transposed = (dt == LA_F32);
@@ -292,9 +352,9 @@ cudaError_t launch_proj(la_dtype dt, const CUtensorMap& tx, const CUtensorMap& t
   switch (dt) {
     case LA_BF16: return launch_p<__nv_bfloat16, 256, 4>(tx, tw, a, st);
     case LA_F16: return launch_p<__half, 256, 4>(tx, tw, a, st);
-    case LA_F32: return launch_p<float, 256, 4>(tx, tw, a, st);
+    case LA_F32: return launch_p<float, 192, 5>(tx, tw, a, st);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace la
