@@ -131,11 +131,13 @@ __device__ __forceinline__ void load_row(uint32_t taddr, uint32_t (&s)[BN]) {
 template <typename T, int BN>
 __device__ __forceinline__ void store_p(uint32_t taddr, uint32_t (&s)[BN]) {
   if constexpr (Elem<T>::tf32) {
-    // round to TF32 (nearest, ties away) with integer ops: a conversion
-    // instruction per element measured ~1000 cycles a row on its slow pipe.
-    // P >= 0 and finite here, so adding half an ulp of TF32 and masking is exact.
+    // Round to TF32 (nearest, ties away): add half a TF32 ulp to the bit
+    // pattern; the kind::tf32 product reads only the top 19 bits of each
+    // 32-bit element, so the low 13 bits need no masking.  P >= 0 and
+    // finite here, so the carry into the exponent is the correct rounding.
+    // (A conversion instruction per element measured ~1000 cycles a row.)
 #pragma unroll
-    for (int c = 0; c < BN; ++c) s[c] = (s[c] + 0x1000u) & 0xFFFFE000u;
+    for (int c = 0; c < BN; ++c) s[c] = s[c] + 0x1000u;
     tmem_st_x64_at<0>(taddr, s);
     if constexpr (BN == 128) tmem_st_x64_at<64>(taddr + 64, s);
   } else {
@@ -171,6 +173,22 @@ __device__ __forceinline__ void store_out32(T* dst, const float (&v)[32]) {
   }
 }
 
+// Packs 128 bytes of output (32 fp32 or 64 half-precision values) into
+// eight 16-byte units; unit u of v.
+template <typename T>
+__device__ __forceinline__ uint4 pack_unit(const float* v, int u) {
+  if constexpr (Elem<T>::tf32) {
+    return make_uint4(f2u(v[4 * u]), f2u(v[4 * u + 1]), f2u(v[4 * u + 2]), f2u(v[4 * u + 3]));
+  } else {
+    uint4 w;
+    w.x = Elem<T>::pack2(v[8 * u + 0], v[8 * u + 1]);
+    w.y = Elem<T>::pack2(v[8 * u + 2], v[8 * u + 3]);
+    w.z = Elem<T>::pack2(v[8 * u + 4], v[8 * u + 5]);
+    w.w = Elem<T>::pack2(v[8 * u + 6], v[8 * u + 7]);
+    return w;
+  }
+}
+
 template <typename T, int D, int NQ, int BN, int NS, int EMU>
 __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -194,32 +212,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- which work this CTA owns ------------------------------------------
-  // Causal: the heaviest query blocks (last rows) go first.
-  const int qblk = a.causal ? (a.num_qblk - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.y;
-  const int b = bh / a.H;
-  const int h = bh - b * a.H;
-  const int split = blockIdx.z;
-  const int off = a.S_kv - a.S_q;  // query row i is absolute position i + off
-  int kv_lim = a.S_kv;
-  if (a.kv_len != nullptr) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
-  const int jb = split * a.tiles_per_split;  // first key tile of this split
-  int je[NQ];                                // one past the last key tile, per query tile
-  int je_all = jb;
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    const int q_lo = (qblk * NQ + t) * kTileM;
-    int n = 0;
-    if (q_lo < a.S_q) {
-      int hi = kv_lim;
-      if (a.causal) hi = min(hi, min(q_lo + kTileM - 1, a.S_q - 1) + off + 1);
-      n = hi > 0 ? (hi + BN - 1) / BN : 0;
-    }
-    je[t] = max(jb, min(n, jb + a.tiles_per_split));
-    je_all = max(je_all, je[t]);
-  }
 
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -249,6 +241,36 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
+  // the set-up above overlaps the previous grid; nothing before this line
+  // reads or writes global memory
+  pdl_wait();
+
+  // ---- which work this CTA owns ------------------------------------------
+  // Causal: the heaviest query blocks (last rows) go first.
+  const int qblk = a.causal ? (a.num_qblk - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int b = bh / a.H;
+  const int h = bh - b * a.H;
+  const int split = blockIdx.z;
+  const int off = a.S_kv - a.S_q;  // query row i is absolute position i + off
+  int kv_lim = a.S_kv;
+  if (a.kv_len != nullptr) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
+  const int jb = split * a.tiles_per_split;  // first key tile of this split
+  int je[NQ];                                // one past the last key tile, per query tile
+  int je_all = jb;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int q_lo = (qblk * NQ + t) * kTileM;
+    int n = 0;
+    if (q_lo < a.S_q) {
+      int hi = kv_lim;
+      if (a.causal) hi = min(hi, min(q_lo + kTileM - 1, a.S_q - 1) + off + 1);
+      n = hi > 0 ? (hi + BN - 1) / BN : 0;
+    }
+    je[t] = max(jb, min(n, jb + a.tiles_per_split));
+    je_all = max(je_all, je[t]);
+  }
+
 
   if (warp == C::WARP_TMA) {
     // ======================= TMA producer ==================================
@@ -506,17 +528,50 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
           if (row_ok) store_out32<float>(a.part_o + prow * D + c0, v);
         }
         if (row_ok) a.part_lse[prow] = l > 0.f ? m_run + __log2f(l) : -INFINITY;
-      } else {
-        T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + static_cast<long long>(q_row) * a.o_ss;
+      } else if (has_o) {
+        // Through shared memory, so that each store instruction writes whole
+        // 128-byte row segments (four rows of the warp per instruction).  The
+        // buffer is this warp's quarter of the query tile's Q buffer: every
+        // QK^T product of this tile completed before o_full, so Q is dead.
+        const uint32_t stg = smem_u32(smem + C::OFF_Q + t * C::Q_TILE + wq * 4096);
+        const int sub = lane >> 3, unit = lane & 7;
+        T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + unit * C::CW / 8;
+        const int r0 = q_lo + wq * 32;  // query row of lane 0
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += C::CW) {
+          float v[C::CW];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          if (has_o) tmem_ld_x32(tO + c0, o);
-          float v[32];
+          for (int hh = 0; hh < C::CW / 32; ++hh) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0 + 32 * hh, o);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = has_o ? u2f(o[c]) * inv : 0.f;
-          if (row_ok) store_out32<T>(dst + c0, v);
+            for (int c = 0; c < 32; ++c) v[32 * hh + c] = u2f(o[c]) * inv;
+          }
+          __syncwarp();  // the previous chunk's reads of the buffer are done
+#pragma unroll
+          for (int u = 0; u < 8; ++u) sts128(stg + lane * 128 + ((u ^ (lane & 7)) << 4), pack_unit<T>(v, u));
+          __syncwarp();
+          uint4 w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {  // row 4i + sub of the warp, this lane's 16-byte unit
+            const int r = 4 * i + sub;
+            w[i] = lds128(stg + r * 128 + ((unit ^ (r & 7)) << 4));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = r0 + 4 * i + sub;
+            if (row < a.S_q) *reinterpret_cast<uint4*>(dst + static_cast<long long>(row) * a.o_ss + c0) = w[i];
+          }
         }
+      } else {
+        // no visible key for any row of this tile: zeros
+        T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + static_cast<long long>(q_row) * a.o_ss;
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32)
+          if (row_ok) store_out32<T>(dst + c0, v);
       }
     }
     __syncthreads();  // teardown rendezvous
@@ -538,9 +593,7 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(a.num_qblk, a.B * a.H, splits);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.num_qblk, a.B * a.H, splits), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, a);
 }
 
 }  // namespace

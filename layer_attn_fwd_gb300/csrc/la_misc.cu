@@ -89,25 +89,54 @@ __global__ void __launch_bounds__(256)
 
 // dst[b][c][r] = src[b][r][c] for 4-byte elements; source rows are C long
 // and batches src_batch apart; destination rows are ld_dst long (>= R) and
-// batches C * ld_dst apart.  32x32 tiles through shared memory, both sides
-// coalesced.
+// batches dst_batch apart.  64x64 tiles through shared memory: each thread
+// keeps four 16-byte loads in flight, and both sides are coalesced.  vec:
+// every row start on both sides is 16-byte aligned (C, ld_dst and the batch
+// strides multiples of 4, bases 16-byte aligned), so 4-wide accesses are
+// used wherever a group of four lies inside the matrix.
 __global__ void __launch_bounds__(256)
     transpose32_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst, int R, int C, long long ld_dst,
-                       long long src_batch, long long dst_batch) {
-  __shared__ uint32_t tile[32][33];
-  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+                       long long src_batch, long long dst_batch, int vec) {
+  __shared__ uint32_t tile[64][65];
+  pdl_trigger();  // the consumer launched next may be scheduled now; it waits for this grid to finish
+  const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
   const long long b = blockIdx.z;
   const uint32_t* s = src + b * src_batch;
   uint32_t* d = dst + b * dst_batch;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + tx;
-    if (r < R && c < C) tile[i][tx] = s[static_cast<long long>(r) * C + c];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16
+  uint32_t v[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + ty + 16 * i, c = c0 + 4 * tx;
+    const uint32_t* p = s + static_cast<long long>(r) * C + c;
+    if (r < R && vec && c + 3 < C) {
+      const uint4 w = *reinterpret_cast<const uint4*>(p);
+      v[i][0] = w.x, v[i][1] = w.y, v[i][2] = w.z, v[i][3] = w.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[i][k] = (r < R && c + k < C) ? p[k] : 0u;
+    }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tile[ty + 16 * i][4 * tx + k] = v[i][k];
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int c = c0 + i, r = r0 + tx;
-    if (r < R && c < C) d[static_cast<long long>(c) * ld_dst + r] = tile[tx][i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c0 + ty + 16 * i, r = r0 + 4 * tx;  // destination row c, columns r .. r+3
+    if (c >= C) continue;
+    uint32_t* p = d + static_cast<long long>(c) * ld_dst + r;
+    const uint32_t w0 = tile[4 * tx][ty + 16 * i], w1 = tile[4 * tx + 1][ty + 16 * i];
+    const uint32_t w2 = tile[4 * tx + 2][ty + 16 * i], w3 = tile[4 * tx + 3][ty + 16 * i];
+    if (vec && r + 3 < R) {
+      *reinterpret_cast<uint4*>(p) = make_uint4(w0, w1, w2, w3);
+    } else {
+      if (r < R) p[0] = w0;
+      if (r + 1 < R) p[1] = w1;
+      if (r + 2 < R) p[2] = w2;
+      if (r + 3 < R) p[3] = w3;
+    }
   }
 }
 
@@ -138,10 +167,13 @@ cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
 cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
                                int R, int C, cudaStream_t st) {
   if (batches == 0 || R == 0 || C == 0) return cudaSuccess;
-  if (batches > 65535 || (C + 31) / 32 > 65535) return cudaErrorInvalidValue;
-  dim3 grid((R + 31) / 32, (C + 31) / 32, static_cast<unsigned>(batches));
+  if (batches > 65535 || (C + 63) / 64 > 65535) return cudaErrorInvalidValue;
+  const long long dst_batch = static_cast<long long>(C) * ld_dst;
+  const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
+                  C % 4 == 0 && ld_dst % 4 == 0 && src_batch % 4 == 0 && dst_batch % 4 == 0;
+  dim3 grid((R + 63) / 64, (C + 63) / 64, static_cast<unsigned>(batches));
   transpose32_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(src), reinterpret_cast<uint32_t*>(dst), R,
-                                            C, ld_dst, src_batch, static_cast<long long>(C) * ld_dst);
+                                            C, ld_dst, src_batch, dst_batch, vec);
   return cudaGetLastError();
 }
 

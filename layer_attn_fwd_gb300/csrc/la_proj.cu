@@ -148,6 +148,10 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
+  // the set-up above overlaps the previous grid; nothing before this line
+  // reads or writes global memory
+  if (threadIdx.x == 0) pdl_trigger();
+  pdl_wait();
 
   if (warp == C::WARP_TMA) {
     int last[NSP];
@@ -234,7 +238,8 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
     // V^T for the fp32 sublayer is stored directly: there lanes hold
     // consecutive positions of one V^T row, which is already coalesced.
     float* sbias = reinterpret_cast<float*>(smem + C::OFF_BIAS) + warp * BNP;
-    uint8_t* stg = smem + C::OFF_STG + warp * C::STG_BYTES;
+    const uint32_t sbias_a = smem_u32(sbias);
+    const uint32_t stg_a = smem_u32(smem + C::OFF_STG + warp * C::STG_BYTES);
     const int d_model = a.K;
     const int sub = lane >> 3, unit = lane & 7;  // row-in-4 and 16-byte unit this lane stores
     int lt = 0;
@@ -253,8 +258,16 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
       const int m = tm * kTileM + warp * 32 + lane;
       const int bidx = m / a.S;
       const int srow = m - bidx * a.S;
-      // element offset of this thread's row inside one [B, H, S, D] output, head 0
+      // element offset of this thread's row inside one [B, H, S, D] output, head 0;
+      // ro[i]: the same for the row this lane stores in step i of each chunk
       const long long row_off = (static_cast<long long>(bidx) * a.H * a.S + srow) * a.D;
+      long long ro[8];
+      bool rok[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ro[i] = __shfl_sync(0xffffffffu, row_off, 4 * i + sub);
+        rok[i] = tm * kTileM + warp * 32 + 4 * i + sub < a.M;
+      }
       const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16) + accb * BNP;
 #pragma unroll 1
       for (int c0 = 0; c0 < BNP; c0 += CW) {
@@ -262,11 +275,12 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
         if (n0 >= a.N) break;  // warp-uniform
         float v[CW];
 #pragma unroll
-        for (int h = 0; h < CW / 32; ++h) {
-          uint32_t acc[32];
-          tmem_ld_x32(trow + c0 + 32 * h, acc);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[32 * h + c] = __uint_as_float(acc[c]);
+        for (int i = 0; i < CW / 4; ++i) {  // bias (same for every row): broadcast loads, issued first
+          const float4 bb = lds128f(sbias_a + (c0 + 4 * i) * 4);
+          v[4 * i] = bb.x;
+          v[4 * i + 1] = bb.y;
+          v[4 * i + 2] = bb.z;
+          v[4 * i + 3] = bb.w;
         }
         const int which = n0 / d_model;
         const int hd = n0 - which * d_model;
@@ -274,7 +288,12 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
         const int dd = hd - hh * a.D;
         const float mul = which == 0 ? a.q_scale : 1.f;
 #pragma unroll
-        for (int c = 0; c < CW; ++c) v[c] = (v[c] + sbias[c0 + c]) * mul;
+        for (int h = 0; h < CW / 32; ++h) {
+          uint32_t acc[32];
+          tmem_ld_x32(trow + c0 + 32 * h, acc);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[32 * h + c] = (__uint_as_float(acc[c]) + v[32 * h + c]) * mul;
+        }
         if (which == 2 && a.v_transposed) {
           // V^T [B, H, D, S_pad]: lanes hold consecutive rows, so each store is coalesced
           if (m < a.M) {
@@ -287,19 +306,19 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
           // row `lane` of the buffer, 16-byte unit u at u ^ lane%8 (conflict-free both ways)
           __syncwarp();  // the previous chunk's reads of the buffer are done
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((u ^ (lane & 7)) << 4)) = pack_unit<T>(v, u);
+          for (int u = 0; u < 8; ++u) sts128(stg_a + lane * 128 + ((u ^ (lane & 7)) << 4), pack_unit<T>(v, u));
           __syncwarp();
-          T* out = reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v));
-          const long long head_off = static_cast<long long>(hh) * a.S * a.D + dd;
+          T* out = reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v)) +
+                   (static_cast<long long>(hh) * a.S * a.D + dd + unit * (16 / C::E));
+          uint4 w[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 4 * i + sub;  // the row this lane stores now
-            const long long ro = __shfl_sync(0xffffffffu, row_off, r);
-            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((unit ^ (r & 7)) << 4));
-            if (tm * kTileM + warp * 32 + r < a.M)
-              *reinterpret_cast<uint4*>(out + ro + head_off + unit * (16 / C::E)) = w;
+          for (int i = 0; i < 8; ++i) {  // row 4i + sub, this lane's 16-byte unit
+            const int r = 4 * i + sub;
+            w[i] = lds128(stg_a + r * 128 + ((unit ^ (r & 7)) << 4));
           }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (rok[i]) *reinterpret_cast<uint4*>(out + ro[i]) = w[i];
         }
       }
       tc_fence_before();
@@ -331,8 +350,7 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArg
   const long long tiles =
       static_cast<long long>((a.N + BNP - 1) / BNP) * ((a.M + kTileM - 1) / kTileM);
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tx, tw, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tx, tw, a);
 }
 
 }  // namespace
