@@ -92,11 +92,16 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + NS * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + NS * KV_TILE;
-  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ], mma_done
-  static constexpr int NBAR = 1 + 4 * NS + 3 * NQ + 1;
+  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ], mma_done,
+  // qt_full
+  static constexpr int NBAR = 1 + 4 * NS + 3 * NQ + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
-  static constexpr int TILE_COLS = BN + D;                 // TMEM columns per query tile: S|P, then O
+  // Q as the A operand of QK^T from tensor memory when it fits: the product
+  // then reads only K from shared memory (half the operand traffic).
+  static constexpr int QCOLS = D * E / 4;                  // 32-bit TMEM columns of one Q row
+  static constexpr bool QT = NQ * (BN + D + QCOLS) <= 512;
+  static constexpr int TILE_COLS = BN + D + (QT ? QCOLS : 0);  // per query tile: S|P, O, then Q
   static constexpr int TMEM_COLS = pow2_at_least(NQ * TILE_COLS);
   static constexpr int QK_STEPS = D * E / 32;              // one MMA consumes 32 bytes of a row
   static constexpr int PV_ROWS = 32 / E;                   // keys per PV MMA (16, or 8 for tf32)
@@ -207,6 +212,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_full = p_full + NQ;
   uint64_t* mma_done = o_full + NQ;
+  uint64_t* qt_full = mma_done + 1;  // Q copied into tensor memory (one arrive per softmax warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -228,6 +234,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       mbar_init(&o_full[t], 1);
     }
     mbar_init(mma_done, 1);
+    mbar_init(qt_full, 4 * NQ);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
       const uint64_t dV = C::VT ? sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024)
                                 : sdesc_sw128(smem_u32(smem + C::OFF_V), C::KV_CHUNK, 1024);
-      bool ok = mbar_wait(q_full, 0, ab, SITE_Q_FULL) && mbar_wait(&k_full[0], 0, ab, SITE_K_FULL);
+      bool ok = mbar_wait(C::QT ? qt_full : q_full, 0, ab, SITE_Q_FULL) && mbar_wait(&k_full[0], 0, ab, SITE_K_FULL);
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -347,7 +354,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
             for (int kk = 0; kk < C::QK_STEPS; ++kk) {
               const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
               const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
-              mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, dK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
+              if constexpr (C::QT)
+                mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + BN + D + kk * 8, dK + off_k, idesc_qk,
+                             kk > 0 ? 1u : 0u);
+              else
+                mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, dK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[t]);
           }
@@ -388,7 +399,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
             for (int kk = 0; kk < C::QK_STEPS; ++kk) {
               const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
               const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
-              mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
+              if constexpr (C::QT)
+                mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + BN + D + kk * 8, bK + off_k, idesc_qk,
+                             kk > 0 ? 1u : 0u);
+              else
+                mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[t]);
           } else {
@@ -429,7 +444,32 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     for (int u = 0; u < NQ; ++u)
       if (u == t) je_t = je[u];
     bool ok = true;
-    for (int j = jb; j < je_t; ++j) {
+    if constexpr (C::QT) {
+      // Copy this thread's Q row (TF32-rounded by the load for fp32; packed
+      // pairs for bf16/fp16) from the swizzled shared tile into tensor-memory
+      // lane `row`, the layout an A operand takes there.
+      if (je_all > jb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, ab, SITE_Q_FULL));
+        if (ok) {
+          const uint32_t qs = smem_u32(smem + C::OFF_Q + t * C::Q_TILE) + row * 128;
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 x = lds128(qs + c * C::Q_CHUNK + ((u ^ (row & 7)) << 4));
+              w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
+            }
+            tmem_st_x32(tO + D + c * 32, w);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qt_full);
+      }
+    }
+    for (int j = jb; ok && j < je_t; ++j) {
       const int i = j - jb;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], i & 1, ab, SITE_S_FULL));
       if (!ok) break;
