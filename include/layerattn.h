@@ -216,8 +216,9 @@ la_status la_get_last_error(la_stream_t st);
 /*
  * The raw device error word read by the latest la_get_last_error() of this
  * process: bit 0 a bounded wait ran out, bit 1 a consistency check failed,
- * bit 8+i wait site i gave up (0 Q loaded, 1 K loaded, 2 V loaded, 3 K slot
- * free, 4 V slot free, 5 scores ready, 6 probabilities ready, 7 output ready,
+ * bit 8+i wait site i gave up (0 Q loaded, 1 K loaded (or the K and V tiles of
+ * a stage, where they share a barrier), 2 V loaded, 3 K slot free, 4 V slot
+ * free, 5 scores ready, 6 probabilities ready, 7 output ready,
  * 8 projection stage loaded, 9 projection stage free, 10 projection
  * accumulator ready, 11 projection accumulator free).  For diagnostics; 0
  * when all was well.

@@ -110,9 +110,19 @@ struct Cfg {
   // head dims, keys contiguous) and a V tile is BN*E/128 chunks of D rows.
   static constexpr bool VT = (E == 4);
   static constexpr int VT_CHUNK = D * 128;
-  static constexpr int THREADS = NQ * 128 + 64;
+  // MMA warps.  With Q in tensor memory, one per query tile, so that one
+  // warp's barrier waits and commits overlap the other's MMA issue
+  // (measured: fp32 D=64 +5%, bf16 D=64 +3%).  With Q in shared memory one
+  // warp, which keeps the strict PV_0, S_0, PV_1, S_1 order (measured: two
+  // warps cost bf16 D=128 10%).
+  static constexpr int MW = QT ? NQ : 1;
+  // One barrier pair per key/value stage (KVM) where measured faster: with Q
+  // in tensor memory (fp32 D=64 +3%, bf16 D=64 +7%); bf16 D=128 with its
+  // two 64 KB stages needs the key slot back before PV is done (-7%).
+  static constexpr bool KVM = QT;
+  static constexpr int THREADS = NQ * 128 + 32 + 32 * MW;
   static constexpr int WARP_TMA = NQ * 4;
-  static constexpr int WARP_MMA = NQ * 4 + 1;
+  static constexpr int WARP_MMA = NQ * 4 + 1;  // first MMA warp
   static_assert(D % CW == 0, "head dim must fill whole 128-byte rows");
   static_assert(TMEM_COLS <= 512, "tensor memory budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -204,6 +214,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
+  // With KVM the key and value tiles of a stage share k_full / k_empty (one
+  // wait and one commit per key tile; v_full / v_empty unused); otherwise K
+  // and V have their own, so that a key slot frees as soon as QK^T is done.
   uint64_t* k_full = q_full + 1;
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
@@ -224,16 +237,16 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], C::MW);  // one commit per MMA warp
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], C::MW);
     }
     for (int t = 0; t < NQ; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);  // one arrive per softmax warp
       mbar_init(&o_full[t], 1);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, C::MW);
     mbar_init(qt_full, 4 * NQ);
     *abort_flag = 0;
     fence_barrier_init();
@@ -300,23 +313,26 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       for (int j = jb; j < je_all; ++j) {
         const int i = j - jb, s = i % NS, r = i / NS;
         if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab, SITE_K_EMPTY)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::KV_TILE);
+        mbar_arrive_expect_tx(&k_full[s], C::KVM ? 2 * C::KV_TILE : C::KV_TILE);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_4d(&tm_k, &k_full[s], smem + C::OFF_K + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
                       j * BN, h, b, pol_kv);
         last_k[s] = r;
-        if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab, SITE_V_EMPTY)) break;
-        mbar_arrive_expect_tx(&v_full[s], C::KV_TILE);
+        uint64_t* vbar = C::KVM ? &k_full[s] : &v_full[s];
+        if constexpr (!C::KVM) {
+          if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab, SITE_V_EMPTY)) break;
+          mbar_arrive_expect_tx(vbar, C::KV_TILE);
+        }
         if constexpr (C::VT) {
           for (int c = 0; c < BN / C::CW; ++c)
-            tma_load_4d(&tm_v, &v_full[s], smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW,
-                        0, h, b, pol_kv);
+            tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW, 0, h,
+                        b, pol_kv);
         } else {
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_4d(&tm_v, &v_full[s], smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
-                        j * BN, h, b, pol_kv);
+            tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW, j * BN, h, b,
+                        pol_kv);
         }
-        last_v[s] = r;
+        if constexpr (!C::KVM) last_v[s] = r;
       }
     }
     __syncwarp();
@@ -330,8 +346,18 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == C::WARP_MMA) {
-    // ======================= MMA issuer ====================================
+  } else if (warp >= C::WARP_MMA) {
+    // ======================= MMA issuers ===================================
+    // MMA warp m issues for query tiles t = m, m + MW, ...  Step j issues
+    // PV(j) and S(j+1).  With KVM, V(j) arrived with K(j) (waited for before
+    // S(j)), stage j+1 is waited for before S(j+1), and stage j is freed at
+    // the end of the step (its K was last read by S(j), its V by PV(j)).
+    // Otherwise V(j) is waited for before PV(j), K(j+1) before S(j+1), and the
+    // V slot of j and the K slot of j+1 are freed at the end of the step.
+    // Every MMA warp waits for and frees every slot use exactly once (the
+    // empty barriers count MW commits), so no warp can run a phase ahead of
+    // another.
+    const int m = warp - C::WARP_MMA;
     if (lane == 0 && je_all > jb) {
       const uint32_t idesc_qk = idesc_make(Elem<T>::ab, kTileM, BN, false, false);
       const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, !C::VT);
@@ -342,37 +368,40 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       const uint64_t dK = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
       const uint64_t dV = C::VT ? sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024)
                                 : sdesc_sw128(smem_u32(smem + C::OFF_V), C::KV_CHUNK, 1024);
+      // S_t = Q_t K^T into the S columns of query tile t (K tile at descriptor bK)
+      auto issue_s = [&](int t, uint64_t bK) {
+        const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+          const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
+          const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
+          if constexpr (C::QT)
+            mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + BN + D + kk * 8, bK + off_k, idesc_qk,
+                         kk > 0 ? 1u : 0u);
+          else
+            mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
       bool ok = mbar_wait(C::QT ? qt_full : q_full, 0, ab, SITE_Q_FULL) && mbar_wait(&k_full[0], 0, ab, SITE_K_FULL);
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) {
+        for (int t = m; t < NQ; t += C::MW) {
           if (je[t] > jb) {
-            // S_t = Q_t K^T: both operands K-major; one MMA per 32 bytes of a row
-            const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-              const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
-              const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
-              if constexpr (C::QT)
-                mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + BN + D + kk * 8, dK + off_k, idesc_qk,
-                             kk > 0 ? 1u : 0u);
-              else
-                mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, dK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
-            }
+            issue_s(t, dK);
             mma_commit(&s_full[t]);
           }
         }
-        mma_commit(&k_empty[0]);
+        if constexpr (!C::KVM) mma_commit(&k_empty[0]);
       }
       for (int j = jb; ok && j < je_all; ++j) {
         const int i = j - jb, s = i % NS, r = i / NS;
         const int sn = (i + 1) % NS, rn = (i + 1) / NS;
         const uint64_t bV = dV + ((s * C::KV_TILE) >> 4);
         const uint64_t bK = dK + ((sn * C::KV_TILE) >> 4);
-        bool v_ready = false, k_next = false;
+        bool v_ready = C::KVM, k_next = false;
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) {
+        for (int t = m; t < NQ; t += C::MW) {
           if (!ok || j >= je[t]) continue;
           ok = mbar_wait(&p_full[t], i & 1, ab, SITE_P_FULL);
           if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
@@ -394,38 +423,44 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
               if (!ok) continue;
               tc_fence_after();
             }
-            const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-              const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
-              const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
-              if constexpr (C::QT)
-                mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + BN + D + kk * 8, bK + off_k, idesc_qk,
-                             kk > 0 ? 1u : 0u);
-              else
-                mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
-            }
+            issue_s(t, bK);
             mma_commit(&s_full[t]);
           } else {
             mma_commit(&o_full[t]);
           }
         }
         if (!ok) break;
-        mma_commit(&v_empty[s]);
-        if (k_next) mma_commit(&k_empty[sn]);
+        if constexpr (C::KVM) {
+          // stage j+1 must be seen full by every MMA warp before stage j is
+          // freed, which keeps each warp's waits in phase order
+          if (j + 1 < je_all && !k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+          if (!ok) break;
+          mma_commit(&k_empty[s]);
+        } else {
+          if (!v_ready) ok = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
+          if (!ok) break;
+          mma_commit(&v_empty[s]);
+          if (j + 1 < je_all) {
+            if (!k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+            if (!ok) break;
+            mma_commit(&k_empty[sn]);
+          }
+        }
       }
     }
     __syncwarp();
     __syncthreads();  // teardown rendezvous
     if (*abort_flag) {
       if (lane == 0) {
-        mma_commit(mma_done);  // fires once every MMA issued so far has finished
+        mma_commit(mma_done);  // fires once every MMA warp's issued MMAs have finished
         mbar_wait_teardown(mma_done, 0);
       }
       __syncwarp();
     }
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == C::WARP_MMA) {  // the warp that allocated
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
   } else {
     // ======================= softmax of query tile t ========================
     const int t = warp >> 2;
