@@ -91,10 +91,11 @@ struct Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * KV_TILE;
-  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ], mma_done,
-  // qt_full
-  static constexpr int NBAR = 1 + 4 * NS + 3 * NQ + 2;
+  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp
+  static constexpr int OFF_BAR = OFF_STG + NQ * 4 * 4096;
+  // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ],
+  // o_free[NQ], mma_done, qt_full
+  static constexpr int NBAR = 2 + 4 * NS + 4 * NQ + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   // Q as the A operand of QK^T from tensor memory when it fits: the product
@@ -204,6 +205,66 @@ __device__ __forceinline__ uint4 pack_unit(const float* v, int u) {
   }
 }
 
+// One work item: the NQ query tiles of query block qblk of head (b, h),
+// against key tiles [jb, je_all) (one split of the key range).
+struct Item {
+  int qblk, b, h, bh, split, kv_lim, jb, je_all;
+};
+
+// Items are numbered with the query block outermost and, when causal, the
+// heaviest block (last rows) first, so that handing them out in order is a
+// longest-first schedule; je[t] is one past the last key tile of query tile
+// t (jb when it has none).
+template <int NQ, int BN>
+__device__ __forceinline__ Item decode_item(const AttnArgs& a, int idx, int (&je)[NQ]) {
+  Item w;
+  const int per_q = a.B * a.H * a.splits;
+  const int qi = idx / per_q;
+  const int rem = idx - qi * per_q;
+  w.bh = rem / a.splits;
+  w.split = rem - w.bh * a.splits;
+  w.qblk = a.causal ? a.num_qblk - 1 - qi : qi;
+  w.b = w.bh / a.H;
+  w.h = w.bh - w.b * a.H;
+  const int off = a.S_kv - a.S_q;  // query row i is absolute position i + off
+  int kv_lim = a.S_kv;
+  if (a.kv_len != nullptr) kv_lim = min(kv_lim, max(a.kv_len[w.b], 0));
+  w.kv_lim = kv_lim;
+  w.jb = w.split * a.tiles_per_split;
+  w.je_all = w.jb;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int q_lo = (w.qblk * NQ + t) * kTileM;
+    int n = 0;
+    if (q_lo < a.S_q) {
+      int hi = kv_lim;
+      if (a.causal) hi = min(hi, min(q_lo + kTileM - 1, a.S_q - 1) + off + 1);
+      n = hi > 0 ? (hi + BN - 1) / BN : 0;
+    }
+    je[t] = max(w.jb, min(n, w.jb + a.tiles_per_split));
+    w.je_all = max(w.je_all, je[t]);
+  }
+  return w;
+}
+
+// je[t] for a t not known at compile time, without indexing local memory.
+template <int NQ>
+__device__ __forceinline__ int sel(const int (&je)[NQ], int t) {
+  int v = je[0];
+#pragma unroll
+  for (int u = 1; u < NQ; ++u)
+    if (u == t) v = je[u];
+  return v;
+}
+
+// Item of round k for CTA c of G: a snake (even rounds left to right, odd
+// rounds right to left), which pairs heavy and light query blocks of a head
+// on one CTA and evens out the work per CTA.
+__device__ __forceinline__ int item_of(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
+
+// Persistent: one CTA per SM walks its items; barrier phases and the
+// key/value ring continue from one item to the next, so an item's loads are
+// issued while the previous item finishes.
 template <typename T, int D, int NQ, int BN, int NS, int EMU>
 __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -214,18 +275,23 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + 1;  // Q in shared memory: the item's last QK^T is done (one MMA commit)
   // With KVM the key and value tiles of a stage share k_full / k_empty (one
   // wait and one commit per key tile; v_full / v_empty unused); otherwise K
   // and V have their own, so that a key slot frees as soon as QK^T is done.
-  uint64_t* k_full = q_full + 1;
+  uint64_t* k_full = q_empty + 1;
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
   uint64_t* s_full = v_empty + NS;
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_full = p_full + NQ;
-  uint64_t* mma_done = o_full + NQ;
+  uint64_t* o_free = o_full + NQ;  // O of query tile t read out (one arrive per softmax warp)
+  uint64_t* mma_done = o_free + NQ;
   uint64_t* qt_full = mma_done + 1;  // Q copied into tensor memory (one arrive per softmax warp)
+  // the Q shared tiles may take the next item's load once: the copy into
+  // tensor memory is done (QT), or the item's last QK^T has completed
+  uint64_t* q_free = C::QT ? qt_full : q_empty;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -235,6 +301,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], C::MW);  // one commit per MMA warp
@@ -245,6 +312,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);  // one arrive per softmax warp
       mbar_init(&o_full[t], 1);
+      mbar_init(&o_free[t], 4);
     }
     mbar_init(mma_done, C::MW);
     mbar_init(qt_full, 4 * NQ);
@@ -265,81 +333,70 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   // reads or writes global memory
   pdl_wait();
 
-  // ---- which work this CTA owns ------------------------------------------
-  // Causal: the heaviest query blocks (last rows) go first.
-  const int qblk = a.causal ? (a.num_qblk - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.y;
-  const int b = bh / a.H;
-  const int h = bh - b * a.H;
-  const int split = blockIdx.z;
+  const int n_items = a.num_qblk * a.B * a.H * a.splits;
+  const int G = gridDim.x, cta = blockIdx.x;
   const int off = a.S_kv - a.S_q;  // query row i is absolute position i + off
-  int kv_lim = a.S_kv;
-  if (a.kv_len != nullptr) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
-  const int jb = split * a.tiles_per_split;  // first key tile of this split
-  int je[NQ];                                // one past the last key tile, per query tile
-  int je_all = jb;
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    const int q_lo = (qblk * NQ + t) * kTileM;
-    int n = 0;
-    if (q_lo < a.S_q) {
-      int hi = kv_lim;
-      if (a.causal) hi = min(hi, min(q_lo + kTileM - 1, a.S_q - 1) + off + 1);
-      n = hi > 0 ? (hi + BN - 1) / BN : 0;
-    }
-    je[t] = max(jb, min(n, jb + a.tiles_per_split));
-    je_all = max(je_all, je[t]);
-  }
-
 
   if (warp == C::WARP_TMA) {
     // ======================= TMA producer ==================================
     int last_k[NS], last_v[NS];
 #pragma unroll
     for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
-    bool q_issued = false;
-    if (lane == 0 && je_all > jb && !a.skip_loads) {
+    int q_last = -1;  // item count of the last Q load issued
+    if (lane == 0 && !a.skip_loads) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
-      for (int t = 0; t < NQ; ++t)
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
-                      (qblk * NQ + t) * kTileM, h, b, pol_q);
-      q_issued = true;
-      for (int j = jb; j < je_all; ++j) {
-        const int i = j - jb, s = i % NS, r = i / NS;
-        if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab, SITE_K_EMPTY)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::KVM ? 2 * C::KV_TILE : C::KV_TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(&tm_k, &k_full[s], smem + C::OFF_K + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
-                      j * BN, h, b, pol_kv);
-        last_k[s] = r;
-        uint64_t* vbar = C::KVM ? &k_full[s] : &v_full[s];
-        if constexpr (!C::KVM) {
-          if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab, SITE_V_EMPTY)) break;
-          mbar_arrive_expect_tx(vbar, C::KV_TILE);
-        }
-        if constexpr (C::VT) {
-          for (int c = 0; c < BN / C::CW; ++c)
-            tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW, 0, h,
-                        b, pol_kv);
-        } else {
+      int it = 0, na = 0;  // key tiles and active items so far
+      bool ok = true;
+      #pragma unroll 1
+      for (int k = 0; ok && k * G < n_items; ++k) {
+        const int idx = item_of(k, cta, G);
+        if (idx >= n_items) continue;
+        int je[NQ];
+        const Item w = decode_item<NQ, BN>(a, idx, je);
+        if (w.je_all <= w.jb) continue;
+        if (na > 0 && !mbar_wait(q_free, (na - 1) & 1, ab, SITE_Q_FULL)) break;
+        mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
+        for (int t = 0; t < NQ; ++t)
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW, j * BN, h, b,
-                        pol_kv);
+            tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
+                        (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
+        q_last = na;
+        for (int j = w.jb; j < w.je_all; ++j, ++it) {
+          const int s = it % NS, r = it / NS;
+          if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab, SITE_K_EMPTY)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[s], C::KVM ? 2 * C::KV_TILE : C::KV_TILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d(&tm_k, &k_full[s], smem + C::OFF_K + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
+                        j * BN, w.h, w.b, pol_kv);
+          last_k[s] = r;
+          uint64_t* vbar = C::KVM ? &k_full[s] : &v_full[s];
+          if constexpr (!C::KVM) {
+            if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, ab, SITE_V_EMPTY)) { ok = false; break; }
+            mbar_arrive_expect_tx(vbar, C::KV_TILE);
+          }
+          if constexpr (C::VT) {
+            for (int c = 0; c < BN / C::CW; ++c)
+              tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW, 0,
+                          w.h, w.b, pol_kv);
+          } else {
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW, j * BN,
+                          w.h, w.b, pol_kv);
+          }
+          if constexpr (!C::KVM) last_v[s] = r;
         }
-        if constexpr (!C::KVM) last_v[s] = r;
+        ++na;
       }
     }
     __syncwarp();
     __syncthreads();  // teardown rendezvous
     if (lane == 0 && *abort_flag) {
       // let the copies still in flight land before the CTA's shared memory goes away
-      if (q_issued) mbar_wait_teardown(q_full, 0);
+      if (q_last >= 0) mbar_wait_teardown(q_full, q_last & 1);
       for (int s = 0; s < NS; ++s) {
         if (last_k[s] >= 0) mbar_wait_teardown(&k_full[s], last_k[s] & 1);
         if (last_v[s] >= 0) mbar_wait_teardown(&v_full[s], last_v[s] & 1);
@@ -356,9 +413,10 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     // V slot of j and the K slot of j+1 are freed at the end of the step.
     // Every MMA warp waits for and frees every slot use exactly once (the
     // empty barriers count MW commits), so no warp can run a phase ahead of
-    // another.
+    // another.  An item's first PV into O waits until the previous item's O
+    // has been read out (o_free).
     const int m = warp - C::WARP_MMA;
-    if (lane == 0 && je_all > jb) {
+    if (lane == 0) {
       const uint32_t idesc_qk = idesc_make(Elem<T>::ab, kTileM, BN, false, false);
       const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, !C::VT);
       // Shared-memory descriptors of the tile bases; the start address field
@@ -382,70 +440,97 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
             mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(C::QT ? qt_full : q_full, 0, ab, SITE_Q_FULL) && mbar_wait(&k_full[0], 0, ab, SITE_K_FULL);
-      if (ok) {
+      constexpr int TPW = NQ / C::MW;  // query tiles per MMA warp: t = m + tt * MW
+      int it = 0, na = 0;
+      int sp[TPW], oc[TPW];  // per own query tile: S/P tiles and outputs so far (barrier phases)
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt) sp[tt] = oc[tt] = 0;
+      bool ok = true;
+      #pragma unroll 1
+      for (int k = 0; ok && k * G < n_items; ++k) {
+        const int idx = item_of(k, cta, G);
+        if (idx >= n_items) continue;
+        int je[NQ];
+        const Item w = decode_item<NQ, BN>(a, idx, je);
+        if (w.je_all <= w.jb) continue;
+        ok = mbar_wait(C::QT ? qt_full : q_full, na & 1, ab, SITE_Q_FULL) &&
+             mbar_wait(&k_full[it % NS], (it / NS) & 1, ab, SITE_K_FULL);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int t = m; t < NQ; t += C::MW) {
-          if (je[t] > jb) {
-            issue_s(t, dK);
+        for (int tt = 0; tt < TPW; ++tt) {
+          const int t = m + tt * C::MW;
+          if (sel(je, t) > w.jb) {
+            issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4));
             mma_commit(&s_full[t]);
           }
         }
-        if constexpr (!C::KVM) mma_commit(&k_empty[0]);
-      }
-      for (int j = jb; ok && j < je_all; ++j) {
-        const int i = j - jb, s = i % NS, r = i / NS;
-        const int sn = (i + 1) % NS, rn = (i + 1) / NS;
-        const uint64_t bV = dV + ((s * C::KV_TILE) >> 4);
-        const uint64_t bK = dK + ((sn * C::KV_TILE) >> 4);
-        bool v_ready = C::KVM, k_next = false;
+        if constexpr (!C::KVM) mma_commit(&k_empty[it % NS]);
+        for (int j = w.jb; ok && j < w.je_all; ++j) {
+          const int i = it + (j - w.jb);
+          const int s = i % NS, r = i / NS;
+          const int sn = (i + 1) % NS, rn = (i + 1) / NS;
+          const uint64_t bV = dV + ((s * C::KV_TILE) >> 4);
+          const uint64_t bK = dK + ((sn * C::KV_TILE) >> 4);
+          bool v_ready = C::KVM, k_next = false;
 #pragma unroll
-        for (int t = m; t < NQ; t += C::MW) {
-          if (!ok || j >= je[t]) continue;
-          ok = mbar_wait(&p_full[t], i & 1, ab, SITE_P_FULL);
-          if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
-          if (!ok) continue;
-          tc_fence_after();
-          // O_t += P_t V: P from tensor memory; V MN-major (rows = keys), or for
-          // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step)
-          const uint32_t d_o = tmem + t * C::TILE_COLS + BN;
-          const uint32_t p_t = tmem + t * C::TILE_COLS;
+          for (int tt = 0; tt < TPW; ++tt) {
+            const int t = m + tt * C::MW;
+            const int je_t = sel(je, t);
+            if (!ok || j >= je_t) continue;
+            ok = mbar_wait(&p_full[t], sp[tt] & 1, ab, SITE_P_FULL);
+            if (ok && j == w.jb && oc[tt] > 0) ok = mbar_wait(&o_free[t], (oc[tt] - 1) & 1, ab, SITE_O_FULL);
+            if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
+            if (!ok) continue;
+            tc_fence_after();
+            ++sp[tt];
+            // O_t += P_t V: P from tensor memory; V MN-major (rows = keys), or for
+            // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step)
+            const uint32_t d_o = tmem + t * C::TILE_COLS + BN;
+            const uint32_t p_t = tmem + t * C::TILE_COLS;
 #pragma unroll
-          for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-            const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
-                                       : (kk * C::PV_ROWS * 128) >> 4;
-            mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > jb || kk > 0) ? 1u : 0u);
-          }
-          if (j + 1 < je[t]) {
-            if (!k_next) {
-              ok = k_next = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
-              if (!ok) continue;
-              tc_fence_after();
+            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+              const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
+                                         : (kk * C::PV_ROWS * 128) >> 4;
+              mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > w.jb || kk > 0) ? 1u : 0u);
             }
-            issue_s(t, bK);
-            mma_commit(&s_full[t]);
+            if (j + 1 < je_t) {
+              if (!k_next) {
+                ok = k_next = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+                if (!ok) continue;
+                tc_fence_after();
+              }
+              issue_s(t, bK);
+              mma_commit(&s_full[t]);
+            } else {
+              mma_commit(&o_full[t]);
+              ++oc[tt];
+            }
+          }
+          if (!ok) break;
+          if constexpr (C::KVM) {
+            // stage j+1 must be seen full by every MMA warp before stage j is
+            // freed, which keeps each warp's waits in phase order
+            if (j + 1 < w.je_all && !k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+            if (!ok) break;
+            mma_commit(&k_empty[s]);
           } else {
-            mma_commit(&o_full[t]);
+            if (!v_ready) ok = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
+            if (!ok) break;
+            mma_commit(&v_empty[s]);
+            if (j + 1 < w.je_all) {
+              if (!k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+              if (!ok) break;
+              mma_commit(&k_empty[sn]);
+            }
           }
         }
         if (!ok) break;
-        if constexpr (C::KVM) {
-          // stage j+1 must be seen full by every MMA warp before stage j is
-          // freed, which keeps each warp's waits in phase order
-          if (j + 1 < je_all && !k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
-          if (!ok) break;
-          mma_commit(&k_empty[s]);
-        } else {
-          if (!v_ready) ok = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
-          if (!ok) break;
-          mma_commit(&v_empty[s]);
-          if (j + 1 < je_all) {
-            if (!k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
-            if (!ok) break;
-            mma_commit(&k_empty[sn]);
-          }
-        }
+        // Q in shared memory: free for the next item's load once this item's
+        // last QK^T (issued above) has completed
+        if constexpr (!C::QT) mma_commit(q_empty);
+        it += w.je_all - w.jb;
+        ++na;
       }
     }
     __syncwarp();
@@ -466,151 +551,177 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const int q_lo = (qblk * NQ + t) * kTileM;
-    const int q_row = q_lo + row;
-    const int r_abs = q_row + off;
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * C::TILE_COLS;
     const uint32_t tO = tS + BN;
-    const float sl2 = a.sl2;
-    float m_run = -INFINITY;  // running max, in log2 units of the scaled scores
-    float l = 0.f;            // running sum of P
-    int je_t = jb;  // this tile's key-tile end, kept in a register
-#pragma unroll
-    for (int u = 0; u < NQ; ++u)
-      if (u == t) je_t = je[u];
+    int sc = 0, oc = 0, na = 0;  // S tiles, outputs and active items so far (barrier phases)
     bool ok = true;
-    if constexpr (C::QT) {
-      // Copy this thread's Q row (TF32-rounded by the load for fp32; packed
-      // pairs for bf16/fp16) from the swizzled shared tile into tensor-memory
-      // lane `row`, the layout an A operand takes there.
-      if (je_all > jb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, ab, SITE_Q_FULL));
+    #pragma unroll 1
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      if (item_of(k, blockIdx.x, gridDim.x) >= n_items) continue;
+      int q_lo, kv_lim, jb, je_t;
+      bool active;
+      {
+        int je[NQ];
+        const Item w = decode_item<NQ, BN>(a, item_of(k, blockIdx.x, gridDim.x), je);
+        q_lo = (w.qblk * NQ + t) * kTileM;
+        kv_lim = w.kv_lim;
+        jb = w.jb;
+        je_t = jb;  // this tile's key-tile end, kept in a register
+#pragma unroll
+        for (int u = 0; u < NQ; ++u)
+          if (u == t) je_t = je[u];
+        active = w.je_all > jb;
+      }
+      const int q_row = q_lo + row;
+      if (C::QT && active) {
+        // Copy this thread's Q row (TF32-rounded by the load for fp32; packed
+        // pairs for bf16/fp16) from the swizzled shared tile into tensor-memory
+        // lane `row`, the layout an A operand takes there.  The previous
+        // item's QK^T products of this tile, which read the old Q there, all
+        // completed before its last scores were read.
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full, na & 1, ab, SITE_Q_FULL));
         if (ok) {
           const uint32_t qs = smem_u32(smem + C::OFF_Q + t * C::Q_TILE) + row * 128;
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
-            uint32_t w[32];
+            uint32_t wv[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const uint4 x = lds128(qs + c * C::Q_CHUNK + ((u ^ (row & 7)) << 4));
-              w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
+              wv[4 * u] = x.x, wv[4 * u + 1] = x.y, wv[4 * u + 2] = x.z, wv[4 * u + 3] = x.w;
             }
-            tmem_st_x32(tO + D + c * 32, w);
+            tmem_st_x32(tO + D + c * 32, wv);
           }
           tmem_st_wait();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(qt_full);
+        if (!ok) break;
       }
-    }
-    for (int j = jb; ok && j < je_t; ++j) {
-      const int i = j - jb;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], i & 1, ab, SITE_S_FULL));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t s[BN];
-      load_row<BN>(tS, s);
-      const int kv0 = j * BN;
-      if (kv0 + BN > kv_lim || (a.causal && kv0 + BN - 1 > q_lo + off)) {
-        int lim = kv_lim;
-        if (a.causal) lim = min(lim, r_abs + 1);
-        lim -= kv0;
+      if (active) ++na;
+      float m_run = -INFINITY;  // running max, in log2 units of the scaled scores
+      float l = 0.f;            // running sum of P
+      for (int j = jb; j < je_t; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sc & 1, ab, SITE_S_FULL));
+        if (!ok) break;
+        ++sc;
+        tc_fence_after();
+        uint32_t s[BN];
+        load_row<BN>(tS, s);
+        const int kv0 = j * BN;
+        if (kv0 + BN > kv_lim || (a.causal && kv0 + BN - 1 > q_lo + off)) {
+          int lim = kv_lim;
+          if (a.causal) lim = min(lim, q_row + off + 1);
+          lim -= kv0;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= lim) s[c] = f2u(-INFINITY);
-      }
-      // row max: 8 independent partial maxima, then a tree (no 128-long
-      // dependency chain)
-      float mxa[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mxa[k] = u2f(s[k]);
-#pragma unroll
-      for (int c = 8; c < BN; c += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(mxa[k], u2f(s[c + k]));
-      const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                             fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const bool grow = m_new > m_run + 8.0f;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ex2_approx(m_run - m_new);  // 0 on the first visible key
-        l *= alpha;
-        m_run = m_new;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float rsa[8];  // row sum: 8 independent partial sums
-#pragma unroll
-      for (int k = 0; k < 8; ++k) rsa[k] = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        // exponent arguments and partial sums two columns per instruction
-        float x0, x1;
-        fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), sl2, sl2, -m_use, -m_use);
-        // the exponentials may be split between the MUFU unit and the FMA pipe
-        const float p0 = (c & 7) < EMU ? ex2_poly(x0) : ex2_approx(x0);
-        const float p1 = ((c + 1) & 7) < EMU ? ex2_poly(x1) : ex2_approx(x1);
-        float& r0 = rsa[c & 7];
-        float& r1 = rsa[(c & 7) + 1];
-        add2(r0, r1, r0, r1, p0, p1);
-        s[c] = f2u(p0);
-        s[c + 1] = f2u(p1);
-      }
-      {
-        float a0, a1, b0, b1;
-        add2(a0, a1, rsa[0], rsa[1], rsa[2], rsa[3]);
-        add2(b0, b1, rsa[4], rsa[5], rsa[6], rsa[7]);
-        add2(a0, a1, a0, a1, b0, b1);
-        l += a0 + a1;
-      }
-      store_p<T, BN>(tS, s);
-      // O was produced by PV of earlier tiles: rescale it to the new max.  The
-      // tensor-memory loads/stores are warp-collective, so the warp rescales
-      // together when any of its rows grew (alpha is 1 for the others).
-      if (__any_sync(0xffffffffu, grow) && j > jb) {
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(tO + c0, o);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = f2u(u2f(o[c]) * alpha);
-          tmem_st_x32(tO + c0, o);
+          for (int c = 0; c < BN; ++c)
+            if (c >= lim) s[c] = f2u(-INFINITY);
         }
+        // row max: 8 independent partial maxima, then a tree (no 128-long
+        // dependency chain)
+        float mxa[8];
+#pragma unroll
+        for (int kq = 0; kq < 8; ++kq) mxa[kq] = u2f(s[kq]);
+#pragma unroll
+        for (int c = 8; c < BN; c += 8)
+#pragma unroll
+          for (int kq = 0; kq < 8; ++kq) mxa[kq] = fmaxf(mxa[kq], u2f(s[c + kq]));
+        const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+        const float m_new = fmaxf(m_run, mx * a.sl2);
+        const bool grow = m_new > m_run + 8.0f;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ex2_approx(m_run - m_new);  // 0 on the first visible key
+          l *= alpha;
+          m_run = m_new;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float rsa[8];  // row sum: 8 independent partial sums
+#pragma unroll
+        for (int kq = 0; kq < 8; ++kq) rsa[kq] = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          // exponent arguments and partial sums two columns per instruction
+          float x0, x1;
+          fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), a.sl2, a.sl2, -m_use, -m_use);
+          // the exponentials may be split between the MUFU unit and the FMA pipe
+          const float p0 = (c & 7) < EMU ? ex2_poly(x0) : ex2_approx(x0);
+          const float p1 = ((c + 1) & 7) < EMU ? ex2_poly(x1) : ex2_approx(x1);
+          float& r0 = rsa[c & 7];
+          float& r1 = rsa[(c & 7) + 1];
+          add2(r0, r1, r0, r1, p0, p1);
+          s[c] = f2u(p0);
+          s[c + 1] = f2u(p1);
+        }
+        {
+          float a0, a1, b0, b1;
+          add2(a0, a1, rsa[0], rsa[1], rsa[2], rsa[3]);
+          add2(b0, b1, rsa[4], rsa[5], rsa[6], rsa[7]);
+          add2(a0, a1, a0, a1, b0, b1);
+          l += a0 + a1;
+        }
+        store_p<T, BN>(tS, s);
+        // O was produced by PV of earlier tiles: rescale it to the new max.  The
+        // tensor-memory loads/stores are warp-collective, so the warp rescales
+        // together when any of its rows grew (alpha is 1 for the others).
+        if (__any_sync(0xffffffffu, grow) && j > jb) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = f2u(u2f(o[c]) * alpha);
+            tmem_st_x32(tO + c0, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
-    }
-    const bool has_o = je_t > jb;
-    if (ok && has_o) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, ab, SITE_O_FULL));
-      if (ok) tc_fence_after();
-    }
-    if (ok) {
+      if (!ok) break;
+      const bool has_o = je_t > jb;
+      if (has_o) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], oc & 1, ab, SITE_O_FULL));
+        if (!ok) break;
+        ++oc;
+        tc_fence_after();
+      }
       const bool row_ok = q_row < a.S_q;
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      int je_unused[NQ];
+      const Item w = decode_item<NQ, BN>(a, item_of(k, blockIdx.x, gridDim.x), je_unused);  // again, for the epilogue
       if (a.part_o != nullptr) {
-        const size_t prow = (static_cast<size_t>(split) * a.B * a.H + bh) * a.S_q + q_row;
+        // split partial: O / l of this split and its log2-sum-exp
+        float* prow = a.part_o + ((static_cast<size_t>(w.split) * a.B * a.H + w.bh) * a.S_q + q_row) * D;
+        if (has_o) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0, o);
+            float v[32];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          if (has_o) tmem_ld_x32(tO + c0, o);
-          float v[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = has_o ? u2f(o[c]) * inv : 0.f;
-          if (row_ok) store_out32<float>(a.part_o + prow * D + c0, v);
+            for (int c = 0; c < 32; ++c) v[c] = u2f(o[c]) * inv;
+            if (row_ok) store_out32<float>(prow + c0, v);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_free[t]);
+        } else if (row_ok) {
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c0 = 0; c0 < D; c0 += 4) *reinterpret_cast<float4*>(prow + c0) = z;
         }
-        if (row_ok) a.part_lse[prow] = l > 0.f ? m_run + __log2f(l) : -INFINITY;
+        if (row_ok)
+          a.part_lse[(static_cast<size_t>(w.split) * a.B * a.H + w.bh) * a.S_q + q_row] =
+              l > 0.f ? m_run + __log2f(l) : -INFINITY;
       } else if (has_o) {
         // Through shared memory, so that each store instruction writes whole
-        // 128-byte row segments (four rows of the warp per instruction).  The
-        // buffer is this warp's quarter of the query tile's Q buffer: every
-        // QK^T product of this tile completed before o_full, so Q is dead.
-        const uint32_t stg = smem_u32(smem + C::OFF_Q + t * C::Q_TILE + wq * 4096);
+        // 128-byte row segments (four rows of the warp per instruction).
+        const uint32_t stg = smem_u32(smem + C::OFF_STG + (t * 4 + wq) * 4096);  // this warp's store box
         const int sub = lane >> 3, unit = lane & 7;
-        T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + unit * C::CW / 8;
+        T* dst = reinterpret_cast<T*>(a.o) + w.b * a.o_sb + w.h * a.o_sh + unit * C::CW / 8;
         const int r0 = q_lo + wq * 32;  // query row of lane 0
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += C::CW) {
@@ -622,25 +733,30 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[32 * hh + c] = u2f(o[c]) * inv;
           }
+          if (c0 + C::CW >= D) {  // O read out: the next item's PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[t]);
+          }
           __syncwarp();  // the previous chunk's reads of the buffer are done
 #pragma unroll
           for (int u = 0; u < 8; ++u) sts128(stg + lane * 128 + ((u ^ (lane & 7)) << 4), pack_unit<T>(v, u));
           __syncwarp();
-          uint4 w[8];
+          uint4 wv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {  // row 4i + sub of the warp, this lane's 16-byte unit
             const int r = 4 * i + sub;
-            w[i] = lds128(stg + r * 128 + ((unit ^ (r & 7)) << 4));
+            wv[i] = lds128(stg + r * 128 + ((unit ^ (r & 7)) << 4));
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int row = r0 + 4 * i + sub;
-            if (row < a.S_q) *reinterpret_cast<uint4*>(dst + static_cast<long long>(row) * a.o_ss + c0) = w[i];
+            const int rr = r0 + 4 * i + sub;
+            if (rr < a.S_q) *reinterpret_cast<uint4*>(dst + static_cast<long long>(rr) * a.o_ss + c0) = wv[i];
           }
         }
       } else {
         // no visible key for any row of this tile: zeros
-        T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + static_cast<long long>(q_row) * a.o_ss;
+        T* dst = reinterpret_cast<T*>(a.o) + w.b * a.o_sb + w.h * a.o_sh + static_cast<long long>(q_row) * a.o_ss;
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = 0.f;
@@ -668,7 +784,15 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return launch_pdl(kern, dim3(a.num_qblk, a.B * a.H, splits), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, a);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(a.num_qblk) * a.B * a.H * splits;
+  if (items == 0) return cudaSuccess;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  AttnArgs b = a;
+  b.splits = splits;
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, b);
 }
 
 }  // namespace

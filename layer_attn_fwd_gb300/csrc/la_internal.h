@@ -44,6 +44,7 @@ struct AttnArgs {
   float sl2;                  // softmax scale times log2(e)
   int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
   int tiles_per_split;        // key tiles handled by one split
+  int splits;                 // key-range splits (set by the launcher)
   uint32_t* err;              // device error word
   int skip_loads;             // test hook: issue no TMA load, so every wait runs out
 };
@@ -58,7 +59,8 @@ struct AttnShape {
 };
 bool attn_shape(la_dtype dt, int D, AttnShape* s);
 
-// Launch the attention kernel over grid (num_qblk, B*H, splits).
+// Launch the persistent attention kernel over its num_qblk * B*H * splits
+// work items (one CTA per SM, at most one per item).
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const AttnArgs& a, int splits, cudaStream_t st);
 
