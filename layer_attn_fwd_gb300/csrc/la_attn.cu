@@ -39,8 +39,15 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "la_device.cuh"
 #include "la_internal.h"
+
+// Work-item ticket counters of the persistent attention kernel: launches
+// take the slots in turn, so that a launch that may overlap the previous one
+// (programmatic dependent launch) never shares its counter.
+__device__ unsigned long long la_sched_ctr[64];
 
 namespace la {
 namespace {
@@ -77,7 +84,10 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <typename T, int D_, int NQ_, int BN_, int NS_, int EMU_>
+// PERS: the persistent form, for launches with more work items than SMs;
+// otherwise each CTA runs exactly one item (no item hand-off, and the
+// epilogue stages its stores in the dead Q tiles).
+template <typename T, int D_, int NQ_, int BN_, int NS_, int EMU_, bool PERS = true>
 struct Cfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, NS = NS_;
   static constexpr int EMU = EMU_;  // of every 8 score columns, how many use the FMA-pipe exp2
@@ -91,13 +101,14 @@ struct Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp
-  static constexpr int OFF_BAR = OFF_STG + NQ * 4 * 4096;
+  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp (PERS)
+  static constexpr int OFF_BAR = OFF_STG + (PERS ? NQ * 4 * 4096 : 0);
   // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ],
-  // o_free[NQ], mma_done, qt_full
-  static constexpr int NBAR = 2 + 4 * NS + 4 * NQ + 2;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+  // o_free[NQ], mma_done, qt_full, item_full[NR], item_empty[NR]
+  static constexpr int NR = 4;  // work items handed from the scheduling thread to the other roles
+  static constexpr int NBAR = 2 + 4 * NS + 4 * NQ + 2 + 2 * NR;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, then the item ring
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 4 * NR + 1024;  // + slack for 1024-byte alignment
   // Q as the A operand of QK^T from tensor memory when it fits: the product
   // then reads only K from shared memory (half the operand traffic).
   static constexpr int QCOLS = D * E / 4;                  // 32-bit TMEM columns of one Q row
@@ -211,18 +222,29 @@ struct Item {
   int qblk, b, h, bh, split, kv_lim, jb, je_all;
 };
 
-// Items are numbered with the query block outermost and, when causal, the
-// heaviest block (last rows) first, so that handing them out in order is a
-// longest-first schedule; je[t] is one past the last key tile of query tile
-// t (jb when it has none).
+// Causal items are numbered with the query block outermost, the heaviest
+// block (last rows) first, so that handing them out in order is a
+// longest-first schedule.  Non-causal items all weigh the same: they are
+// numbered head by head, so that the query blocks of a head (which read the
+// same keys and values) run side by side.  Key-range splits are innermost.
+// je[t] is one past the last key tile of query tile t (jb when it has none).
 template <int NQ, int BN>
 __device__ __forceinline__ Item decode_item(const AttnArgs& a, int idx, int (&je)[NQ]) {
   Item w;
-  const int per_q = a.B * a.H * a.splits;
-  const int qi = idx / per_q;
-  const int rem = idx - qi * per_q;
-  w.bh = rem / a.splits;
-  w.split = rem - w.bh * a.splits;
+  int qi;
+  if (a.causal) {
+    const int per_q = a.B * a.H * a.splits;
+    qi = idx / per_q;
+    const int rem = idx - qi * per_q;
+    w.bh = rem / a.splits;
+    w.split = rem - w.bh * a.splits;
+  } else {
+    const int per_bh = a.num_qblk * a.splits;
+    w.bh = idx / per_bh;
+    const int rem = idx - w.bh * per_bh;
+    qi = rem / a.splits;
+    w.split = rem - qi * a.splits;
+  }
   w.qblk = a.causal ? a.num_qblk - 1 - qi : qi;
   w.b = w.bh / a.H;
   w.h = w.bh - w.b * a.H;
@@ -257,19 +279,19 @@ __device__ __forceinline__ int sel(const int (&je)[NQ], int t) {
   return v;
 }
 
-// Item of round k for CTA c of G: a snake (even rounds left to right, odd
-// rounds right to left), which pairs heavy and light query blocks of a head
-// on one CTA and evens out the work per CTA.
-__device__ __forceinline__ int item_of(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
-
-// Persistent: one CTA per SM walks its items; barrier phases and the
-// key/value ring continue from one item to the next, so an item's loads are
-// issued while the previous item finishes.
-template <typename T, int D, int NQ, int BN, int NS, int EMU>
-__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
+// Persistent: one CTA per SM.  CTA c starts with item c; further items come
+// from a global ticket counter (heaviest first, whichever CTA is free next),
+// ticket t meaning item gridDim.x + t.  Barrier phases and the key/value
+// ring continue from one item to the next, so an item's loads are issued
+// while the previous item finishes.  Ticket t of a launch is *a.sched -
+// a.sched_base; every CTA draws until it gets one past the last item, so a
+// launch draws exactly as many tickets as it has items (the host advances
+// the base by that much).
+template <typename T, int D, int NQ, int BN, int NS, int EMU, bool PERS>
+__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using C = Cfg<T, D, NQ, BN, NS, EMU>;
+  using C = Cfg<T, D, NQ, BN, NS, EMU, PERS>;
   constexpr bool TF32 = Elem<T>::tf32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,11 +311,14 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   uint64_t* o_free = o_full + NQ;  // O of query tile t read out (one arrive per softmax warp)
   uint64_t* mma_done = o_free + NQ;
   uint64_t* qt_full = mma_done + 1;  // Q copied into tensor memory (one arrive per softmax warp)
+  uint64_t* item_full = qt_full + 1;  // ring slot holds the next item (-1: none left)
+  uint64_t* item_empty = item_full + C::NR;  // every consumer warp has read the slot
   // the Q shared tiles may take the next item's load once: the copy into
   // tensor memory is done (QT), or the item's last QK^T has completed
   uint64_t* q_free = C::QT ? qt_full : q_empty;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -316,6 +341,10 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     }
     mbar_init(mma_done, C::MW);
     mbar_init(qt_full, 4 * NQ);
+    for (int r = 0; r < C::NR; ++r) {
+      mbar_init(&item_full[r], 1);
+      mbar_init(&item_empty[r], C::MW + 4 * NQ);  // MMA warps and softmax warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -334,8 +363,21 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   pdl_wait();
 
   const int n_items = a.num_qblk * a.B * a.H * a.splits;
-  const int G = gridDim.x, cta = blockIdx.x;
   const int off = a.S_kv - a.S_q;  // query row i is absolute position i + off
+  // The next item from the ring (consumer side): -1 when none is left or a
+  // wait ran out.  Called by a whole converged warp (softmax) or by lane 0
+  // alone (MMA issuers); one arrive per warp frees the slot.
+  auto next_item = [&](int& n_taken, bool whole_warp) -> int {
+    const int rs = n_taken % C::NR, rr = n_taken / C::NR;
+    ++n_taken;
+    bool got = mbar_wait(&item_full[rs], rr & 1, ab, SITE_Q_FULL);
+    if (whole_warp) got = __all_sync(0xffffffffu, got);
+    if (!got) return -1;
+    const int idx = ring[rs];
+    if (whole_warp) __syncwarp();
+    if (lane == 0) mbar_arrive(&item_empty[rs]);
+    return idx;
+  };
 
   if (warp == C::WARP_TMA) {
     // ======================= TMA producer ==================================
@@ -343,28 +385,67 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
 #pragma unroll
     for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
     int q_last = -1;  // item count of the last Q load issued
-    if (lane == 0 && !a.skip_loads) {
-      tma_prefetch_desc(&tm_q);
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_first();
+      // The first item's Q goes out before anything else: after an L2 flush
+      // the first instructions of this path miss in the instruction cache,
+      // and everything issued ahead of the load delays it.
+      bool q_pre = false;
+      {
+        int je0[NQ];
+        const Item w0 = decode_item<NQ, BN>(a, blockIdx.x, je0);
+        if (w0.je_all > w0.jb && !a.skip_loads) {
+          mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
+          for (int t = 0; t < NQ; ++t)
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
+                          (w0.qblk * NQ + t) * kTileM, w0.h, w0.b, pol_q);
+          q_pre = true;
+          q_last = 0;
+        }
+      }
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      int it = 0, na = 0;  // key tiles and active items so far
-      bool ok = true;
-      #pragma unroll 1
-      for (int k = 0; ok && k * G < n_items; ++k) {
-        const int idx = item_of(k, cta, G);
-        if (idx >= n_items) continue;
+      const int G = gridDim.x;
+      // (with no more items than CTAs there is nothing to hand out: no ticket
+      // is drawn and the launcher reserves none)
+      auto draw = [&]() -> int {
+        if (!PERS || n_items <= G || a.sched == nullptr) return -1;
+        const unsigned long long tk = atomicAdd(a.sched, 1ull) - a.sched_base;
+        return tk < static_cast<unsigned long long>(n_items - G) ? G + static_cast<int>(tk) : -1;
+      };
+      int it = 0, na = 0, nr = 0;  // key tiles, active items and ring slots so far
+      bool ok = true, drawn_last = false, first = true;
+#pragma unroll 1
+      while (ok) {
+        if (!PERS && !first) break;
+        int idx = blockIdx.x;  // the first item needs no ticket and no hand-off
+        if (!first) {
+          idx = draw();
+          drawn_last = idx < 0;
+          const int rs = nr % C::NR, rr = nr / C::NR;
+          ++nr;
+          if (rr > 0 && !mbar_wait(&item_empty[rs], (rr - 1) & 1, ab, SITE_Q_FULL)) break;
+          ring[rs] = idx;
+          mbar_arrive(&item_full[rs]);  // releases the slot write to the waiting warps
+          if (idx < 0) break;
+        }
+        first = false;
         int je[NQ];
         const Item w = decode_item<NQ, BN>(a, idx, je);
-        if (w.je_all <= w.jb) continue;
-        if (na > 0 && !mbar_wait(q_free, (na - 1) & 1, ab, SITE_Q_FULL)) break;
-        mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
-        for (int t = 0; t < NQ; ++t)
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
-                        (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
-        q_last = na;
+        if (w.je_all <= w.jb || a.skip_loads) continue;
+        if (q_pre) {
+          q_pre = false;  // the first item's Q is already on its way
+        } else {
+          if (na > 0 && !mbar_wait(q_free, (na - 1) & 1, ab, SITE_Q_FULL)) break;
+          mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
+          for (int t = 0; t < NQ; ++t)
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
+                          (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
+          q_last = na;
+        }
         for (int j = w.jb; j < w.je_all; ++j, ++it) {
           const int s = it % NS, r = it / NS;
           if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab, SITE_K_EMPTY)) { ok = false; break; }
@@ -391,6 +472,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
         }
         ++na;
       }
+      // a CTA that stopped early still draws until the end of the items, so
+      // that this launch consumes exactly items + CTAs tickets
+      if (PERS && !drawn_last)
+        while (draw() >= 0) {
+        }
     }
     __syncwarp();
     __syncthreads();  // teardown rendezvous
@@ -446,10 +532,13 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
 #pragma unroll
       for (int tt = 0; tt < TPW; ++tt) sp[tt] = oc[tt] = 0;
       bool ok = true;
-      #pragma unroll 1
-      for (int k = 0; ok && k * G < n_items; ++k) {
-        const int idx = item_of(k, cta, G);
-        if (idx >= n_items) continue;
+      int taken = -1;
+#pragma unroll 1
+      while (ok) {
+        if (!PERS && taken >= 0) break;
+        const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, false);
+        if (taken < 0) taken = 0;
+        if (idx < 0) break;
         int je[NQ];
         const Item w = decode_item<NQ, BN>(a, idx, je);
         if (w.je_all <= w.jb) continue;
@@ -554,15 +643,19 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * C::TILE_COLS;
     const uint32_t tO = tS + BN;
     int sc = 0, oc = 0, na = 0;  // S tiles, outputs and active items so far (barrier phases)
+    int taken = -1;
     bool ok = true;
-    #pragma unroll 1
-    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-      if (item_of(k, blockIdx.x, gridDim.x) >= n_items) continue;
+#pragma unroll 1
+    while (ok) {
+      if (!PERS && taken >= 0) break;
+      const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, true);
+      if (taken < 0) taken = 0;
+      if (idx < 0) break;
       int q_lo, kv_lim, jb, je_t;
       bool active;
       {
         int je[NQ];
-        const Item w = decode_item<NQ, BN>(a, item_of(k, blockIdx.x, gridDim.x), je);
+        const Item w = decode_item<NQ, BN>(a, idx, je);
         q_lo = (w.qblk * NQ + t) * kTileM;
         kv_lim = w.kv_lim;
         jb = w.jb;
@@ -692,7 +785,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       const bool row_ok = q_row < a.S_q;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       int je_unused[NQ];
-      const Item w = decode_item<NQ, BN>(a, item_of(k, blockIdx.x, gridDim.x), je_unused);  // again, for the epilogue
+      const Item w = decode_item<NQ, BN>(a, idx, je_unused);  // again, for the epilogue
       if (a.part_o != nullptr) {
         // split partial: O / l of this split and its log2-sum-exp
         float* prow = a.part_o + ((static_cast<size_t>(w.split) * a.B * a.H + w.bh) * a.S_q + q_row) * D;
@@ -719,7 +812,10 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
       } else if (has_o) {
         // Through shared memory, so that each store instruction writes whole
         // 128-byte row segments (four rows of the warp per instruction).
-        const uint32_t stg = smem_u32(smem + C::OFF_STG + (t * 4 + wq) * 4096);  // this warp's store box
+        // this warp's 4 KB store box (single-item form: a quarter of the query
+        // tile's Q buffer, dead since every QK^T of the tile completed)
+        const uint32_t stg =
+            smem_u32(smem + (PERS ? C::OFF_STG + (t * 4 + wq) * 4096 : C::OFF_Q + t * C::Q_TILE + wq * 4096));
         const int sub = lane >> 3, unit = lane & 7;
         T* dst = reinterpret_cast<T*>(a.o) + w.b * a.o_sb + w.h * a.o_sh + unit * C::CW / 8;
         const int r0 = q_lo + wq * 32;  // query row of lane 0
@@ -769,11 +865,37 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU>::THREADS, 1)
   }
 }
 
-template <typename T, int D, int NQ, int BN, int NS, int EMU>
-cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
-                       int splits, cudaStream_t st) {
-  using C = Cfg<T, D, NQ, BN, NS, EMU>;
-  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, EMU>;
+// Counter slot and its starting value for a launch that will draw `tickets`.
+cudaError_t sched_slot(long long tickets, unsigned long long** ctr, unsigned long long* base) {
+  constexpr int kDev = 64, kSlots = 64;
+  static std::mutex mu;
+  static unsigned long long* addr[kDev] = {};
+  static unsigned long long next_base[kDev][kSlots] = {};
+  static int next_slot[kDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, la_sched_ctr);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned long long*>(p);
+  }
+  const int slot = next_slot[dev];
+  next_slot[dev] = (slot + 1) % kSlots;
+  *ctr = addr[dev] + slot;
+  *base = next_base[dev][slot];
+  next_base[dev][slot] += static_cast<unsigned long long>(tickets);
+  return cudaSuccess;
+}
+
+template <typename T, int D, int NQ, int BN, int NS, int EMU, bool PERS>
+cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& b,
+                        int grid, cudaStream_t st) {
+  using C = Cfg<T, D, NQ, BN, NS, EMU, PERS>;
+  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, EMU, PERS>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -784,15 +906,27 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  int sms = 0;
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, b);
+}
+
+// One CTA per item when the items fit on the SMs at once; otherwise the
+// persistent form on every SM, drawing items by ticket.
+template <typename T, int D, int NQ, int BN, int NS, int EMU>
+cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                       int splits, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(a.num_qblk) * a.B * a.H * splits;
   if (items == 0) return cudaSuccess;
-  const int grid = static_cast<int>(items < sms ? items : sms);
   AttnArgs b = a;
   b.splits = splits;
-  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, b);
+  if (items <= sms) return launch_form<T, D, NQ, BN, NS, EMU, false>(tq, tk, tv, b, static_cast<int>(items), st);
+  e = sched_slot(items, &b.sched, &b.sched_base);
+  if (e != cudaSuccess) return e;
+  return launch_form<T, D, NQ, BN, NS, EMU, true>(tq, tk, tv, b, sms, st);
 }
 
 }  // namespace

@@ -45,6 +45,8 @@ struct AttnArgs {
   int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
   int tiles_per_split;        // key tiles handled by one split
   int splits;                 // key-range splits (set by the launcher)
+  unsigned long long* sched;  // work-item ticket counter (set by the launcher)
+  unsigned long long sched_base;  // its value when this launch starts
   uint32_t* err;              // device error word
   int skip_loads;             // test hook: issue no TMA load, so every wait runs out
 };
