@@ -642,17 +642,44 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     const int row = wq * 32 + lane;
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * C::TILE_COLS;
     const uint32_t tO = tS + BN;
-    int sc = 0, oc = 0, na = 0;  // S tiles, outputs and active items so far (barrier phases)
-    int taken = -1;
+    int sc = 0, oc = 0, na = 0;  // S tiles, outputs and Q copies so far (barrier phases)
     bool ok = true;
+    // Copy this thread's Q row of item idx (TF32-rounded by the load for
+    // fp32; packed pairs for bf16/fp16) from the swizzled shared tile into
+    // tensor-memory lane `row`, the layout an A operand takes there.  The
+    // previous item's QK^T products of this tile, which read the old Q there,
+    // all completed before its last scores were read.
+    auto copy_q = [&](int idx) -> bool {
+      int je[NQ];
+      const Item w = decode_item<NQ, BN>(a, idx, je);
+      if (!C::QT || w.je_all <= w.jb) return true;
+      bool good = __all_sync(0xffffffffu, mbar_wait(q_full, na & 1, ab, SITE_Q_FULL));
+      if (good) {
+        const uint32_t qs = smem_u32(smem + C::OFF_Q + t * C::Q_TILE) + row * 128;
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = lds128(qs + c * C::Q_CHUNK + ((u ^ (row & 7)) << 4));
+            wv[4 * u] = x.x, wv[4 * u + 1] = x.y, wv[4 * u + 2] = x.z, wv[4 * u + 3] = x.w;
+          }
+          tmem_st_x32(tO + D + c * 32, wv);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qt_full);
+      ++na;
+      return good;
+    };
+    int taken = 0;
+    int idx = blockIdx.x;  // the first item needs no hand-off
+    ok = copy_q(idx);
 #pragma unroll 1
     while (ok) {
-      if (!PERS && taken >= 0) break;
-      const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, true);
-      if (taken < 0) taken = 0;
-      if (idx < 0) break;
       int q_lo, kv_lim, jb, je_t;
-      bool active;
       {
         int je[NQ];
         const Item w = decode_item<NQ, BN>(a, idx, je);
@@ -663,36 +690,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
 #pragma unroll
         for (int u = 0; u < NQ; ++u)
           if (u == t) je_t = je[u];
-        active = w.je_all > jb;
       }
       const int q_row = q_lo + row;
-      if (C::QT && active) {
-        // Copy this thread's Q row (TF32-rounded by the load for fp32; packed
-        // pairs for bf16/fp16) from the swizzled shared tile into tensor-memory
-        // lane `row`, the layout an A operand takes there.  The previous
-        // item's QK^T products of this tile, which read the old Q there, all
-        // completed before its last scores were read.
-        ok = __all_sync(0xffffffffu, mbar_wait(q_full, na & 1, ab, SITE_Q_FULL));
-        if (ok) {
-          const uint32_t qs = smem_u32(smem + C::OFF_Q + t * C::Q_TILE) + row * 128;
-#pragma unroll
-          for (int c = 0; c < C::NCH; ++c) {
-            uint32_t wv[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 x = lds128(qs + c * C::Q_CHUNK + ((u ^ (row & 7)) << 4));
-              wv[4 * u] = x.x, wv[4 * u + 1] = x.y, wv[4 * u + 2] = x.z, wv[4 * u + 3] = x.w;
-            }
-            tmem_st_x32(tO + D + c * 32, wv);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qt_full);
-        if (!ok) break;
-      }
-      if (active) ++na;
       float m_run = -INFINITY;  // running max, in log2 units of the scaled scores
       float l = 0.f;            // running sum of P
       for (int j = jb; j < je_t; ++j) {
@@ -774,6 +773,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[t]);
       }
+      if (!ok) break;
+      // The next item's Q goes into tensor memory before this item's output
+      // is read out, so that its first QK^T runs during this epilogue.
+      const int next = PERS ? next_item(taken, true) : -1;
+      if (next >= 0) ok = copy_q(next);
       if (!ok) break;
       const bool has_o = je_t > jb;
       if (has_o) {
@@ -860,6 +864,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         for (int c0 = 0; c0 < D; c0 += 32)
           if (row_ok) store_out32<T>(dst + c0, v);
       }
+      if (next < 0) break;
+      idx = next;
     }
     __syncthreads();  // teardown rendezvous
   }
