@@ -358,8 +358,14 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
-  // the set-up above overlaps the previous grid; nothing before this line
-  // reads or writes global memory
+  // The set-up above overlaps the previous grid; nothing before the wait
+  // reads or writes global memory the previous grid may touch.  The tensor
+  // maps are kernel parameters, so their descriptors are fetched meanwhile.
+  if (warp == C::WARP_TMA && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
   pdl_wait();
 
   const int n_items = a.num_qblk * a.B * a.H * a.splits;
@@ -404,8 +410,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
           q_last = 0;
         }
       }
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       const uint64_t pol_kv = policy_evict_last();
       const int G = gridDim.x;
       // (with no more items than CTAs there is nothing to hand out: no ticket

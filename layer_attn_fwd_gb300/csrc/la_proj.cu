@@ -148,9 +148,14 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{a.err, abort_flag};
-  // the set-up above overlaps the previous grid; nothing before this line
-  // reads or writes global memory
+  // The set-up above overlaps the previous grid; nothing before the wait
+  // reads or writes global memory the previous grid may touch.  The tensor
+  // maps are kernel parameters, so their descriptors are fetched meanwhile.
   if (threadIdx.x == 0) pdl_trigger();
+  if (warp == C::WARP_TMA && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+  }
   pdl_wait();
 
   if (warp == C::WARP_TMA) {
@@ -158,8 +163,6 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
 #pragma unroll
     for (int s = 0; s < NSP; ++s) last[s] = -1;
     if (lane == 0) {
-      tma_prefetch_desc(&tm_x);
-      tma_prefetch_desc(&tm_w);
       const uint64_t pol_x = policy_evict_first();
       const uint64_t pol_w = policy_evict_last();
       int it = 0;
