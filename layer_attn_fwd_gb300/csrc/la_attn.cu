@@ -39,15 +39,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <mutex>
-
 #include "la_device.cuh"
 #include "la_internal.h"
-
-// Work-item ticket counters of the persistent attention kernel: launches
-// take the slots in turn, so that a launch that may overlap the previous one
-// (programmatic dependent launch) never shares its counter.
-__device__ unsigned long long la_sched_ctr[64];
 
 namespace la {
 namespace {
@@ -875,32 +868,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
   }
 }
 
-// Counter slot and its starting value for a launch that will draw `tickets`.
-cudaError_t sched_slot(long long tickets, unsigned long long** ctr, unsigned long long* base) {
-  constexpr int kDev = 64, kSlots = 64;
-  static std::mutex mu;
-  static unsigned long long* addr[kDev] = {};
-  static unsigned long long next_base[kDev][kSlots] = {};
-  static int next_slot[kDev] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kDev) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, la_sched_ctr);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<unsigned long long*>(p);
-  }
-  const int slot = next_slot[dev];
-  next_slot[dev] = (slot + 1) % kSlots;
-  *ctr = addr[dev] + slot;
-  *base = next_base[dev][slot];
-  next_base[dev][slot] += static_cast<unsigned long long>(tickets);
-  return cudaSuccess;
-}
-
 template <typename T, int D, int NQ, int BN, int NS, int EMU, bool PERS>
 cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& b,
                         int grid, cudaStream_t st) {
@@ -934,7 +901,7 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   AttnArgs b = a;
   b.splits = splits;
   if (items <= sms) return launch_form<T, D, NQ, BN, NS, EMU, false>(tq, tk, tv, b, static_cast<int>(items), st);
-  e = sched_slot(items, &b.sched, &b.sched_base);
+  e = counter_slot(items, &b.sched, &b.sched_base);
   if (e != cudaSuccess) return e;
   return launch_form<T, D, NQ, BN, NS, EMU, true>(tq, tk, tv, b, sms, st);
 }

@@ -66,6 +66,11 @@ bool attn_shape(la_dtype dt, int D, AttnShape* s);
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const AttnArgs& a, int splits, cudaStream_t st);
 
+// A slot of the device's monotonic counters (attention work tickets) for a
+// launch that will add `tickets` to it; *base is the slot's value when the
+// launch starts.
+cudaError_t counter_slot(long long tickets, unsigned long long** ctr, unsigned long long* base);
+
 // Merge split partials into o.
 struct CombineArgs {
   const float* part_o;

@@ -12,8 +12,15 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "la_device.cuh"
 #include "la_internal.h"
+
+// Monotonic device counters (the attention's work tickets).  Launches take
+// the slots in turn, so that a launch that may overlap the previous one
+// (programmatic dependent launch) never shares one.
+__device__ unsigned long long la_counters[64];
 
 namespace la {
 namespace {
@@ -148,6 +155,31 @@ int sm_count() {
 }
 
 }  // namespace
+
+cudaError_t counter_slot(long long tickets, unsigned long long** ctr, unsigned long long* base) {
+  constexpr int kDev = 64, kSlots = 64;
+  static std::mutex mu;
+  static unsigned long long* addr[kDev] = {};
+  static unsigned long long next_base[kDev][kSlots] = {};
+  static int next_slot[kDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, la_counters);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned long long*>(p);
+  }
+  const int slot = next_slot[dev];
+  next_slot[dev] = (slot + 1) % kSlots;
+  *ctr = addr[dev] + slot;
+  *base = next_base[dev][slot];
+  next_base[dev][slot] += static_cast<unsigned long long>(tickets);
+  return cudaSuccess;
+}
 
 cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
   const long long total = static_cast<long long>(a.B) * a.H * a.S_q * (a.D / 4);
