@@ -7,26 +7,35 @@
 // equation of "Shape-Aware Attention" (section Inspiration), with causal and
 // key-padding masks.
 //
-// One CTA owns NQ query tiles of 128 rows of one (batch, head) and walks a
-// range of 128-key tiles (the whole causal/padded range, or one split of it):
+// A work item is NQ query tiles of 128 rows of one (batch, head) against a
+// range of 128-key tiles (the whole causal/padded range, or one split of it).
+// With no more items than SMs each CTA runs one item; otherwise one CTA per
+// SM takes items by ticket (the persistent form).  Roles in a CTA:
 //
-//   warp 4*NQ   (TMA)      loads Q once, then K_j / V_j through an NS-stage
-//                          ring of shared-memory buffers (128-byte swizzle).
-//                          For fp32 (TF32 products, which take K-major
-//                          operands only) V comes from its transpose V^T.
-//   warp 4*NQ+1 (MMA)      one thread issues tcgen05.mma:  S_t = Q_t K_j^T into
-//                          tensor memory, then O_t += P_t V_j with P_t read
-//                          straight from tensor memory (A operand in TMEM).
+//   warp 4*NQ   (TMA)      loads Q, then K_j / V_j through an NS-stage ring
+//                          of shared-memory buffers (128-byte swizzle), and
+//                          in the persistent form draws the items and hands
+//                          them to the other warps.  For fp32 (TF32
+//                          products, which take K-major operands only) V
+//                          comes from its transpose V^T.
+//   warps 4*NQ+1..         tcgen05.mma issuers (one, or one per query tile
+//   (MMA)                  where Q sits in tensor memory):  S_t = Q_t K_j^T
+//                          into tensor memory, then O_t += P_t V_j with P_t
+//                          read straight from tensor memory (A operand in
+//                          TMEM).
 //   warps 4t..4t+3         softmax of query tile t: thread r owns row r of
 //   (softmax, tile t)      S_t (tcgen05.ld 32x32b), applies the mask, keeps
 //                          the running max m and sum l in registers, writes
 //                          P = exp2(S*scale*log2e - m) back over S (bf16/f16
 //                          packed pairs, or tf32), and rescales O_t in tensor
 //                          memory when the max grows; finally O_t / l -> HBM.
+//                          Where it fits they first copy Q_t into tensor
+//                          memory, so that QK^T reads only K from shared
+//                          memory.
 //
 // The two query tiles ping-pong: while tile 0's softmax runs, the tensor core
 // computes PV and the next QK^T of tile 1, and vice versa.  Per tile the MMA
-// thread issues PV_t(j) before S_t(j+1), so when the softmax sees S_t(j+1)
+// issue order is PV_t(j) before S_t(j+1), so when the softmax sees S_t(j+1)
 // complete, PV_t(j) is complete as well; the O rescale and the P overwrite
 // need no other wait.
 //
