@@ -41,6 +41,20 @@ def layer_inputs(B, S, d_model, dtype=torch.float32, seed=0, bias="zero"):
     return x.to(dtype), W.to(dtype), b.to(dtype)
 
 
+def out_proj_inputs(d_model, dtype=torch.float32, seed=0, bias="zero"):
+    """Output projection weight Wo [d,d] ~ N(0,1/d) and bias bo [d], zero or
+    N(0,1/4)."""
+    g = _gen(seed)
+    Wo = torch.randn(d_model, d_model, generator=g, dtype=torch.float32) / (d_model ** 0.5)
+    if bias == "zero":
+        bo = torch.zeros(d_model, dtype=torch.float32)
+    elif bias == "normal":
+        bo = 0.5 * torch.randn(d_model, generator=g, dtype=torch.float32)
+    else:
+        raise ValueError(bias)
+    return Wo.to(dtype), bo.to(dtype)
+
+
 def padding_kv_len(B, S_kv):
     """Key-padding pattern: the first half of the batch keeps 75% of its keys
     (the last quarter is padding); the second half keeps all of them."""

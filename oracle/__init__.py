@@ -57,6 +57,8 @@ def _load():
             lib.oracle_attn_chunked.argtypes = [P, P, P, I, P, I, I, LL, I, I, D, LL]
             lib.oracle_qkv_proj.argtypes = [P, P, P, I, P, P, P, I, LL, I, I, D]
             lib.oracle_layer_attn.argtypes = [P, P, P, I, P, I, LL, I, I, I, P]
+            lib.oracle_out_proj.argtypes = [P, I, P, P, I, P, LL, I, I]
+            lib.oracle_layer_attn_out.argtypes = [P, P, P, P, P, I, P, I, LL, I, I, I, P]
             lib.oracle_widen.argtypes = [P, I, LL]
             lib.oracle_widen.restype = D
             lib.oracle_num_threads.restype = I
@@ -232,6 +234,41 @@ def layer_attn(x, W, bias, H, causal=False, kv_len=None):
     _check(_load().oracle_layer_attn(_ptr(xb), _ptr(wb), _ptr(bb), dt, _ptr(o), B, S, dm, H,
                                      int(bool(causal)), _ptr(kl)), "layer_attn")
     return o
+
+
+def out_proj(a, W, bias=None):
+    """a [..., d_in] (any supported type), W [d_in, d_out], bias [d_out] or
+    None -> a W + bias in fp64, shape [..., d_out]."""
+    ab, dta = _as_buffer(a)
+    if bias is None:
+        (wb,), dtw = _same_type(W)
+        bb = None
+    else:
+        (wb, bb), dtw = _same_type(W, bias)
+    d_in, d_out = wb.shape
+    if ab.shape[-1] != d_in:
+        raise ValueError("oracle: a and W disagree on d_in")
+    M = ab.size // d_in
+    y = np.zeros(ab.shape[:-1] + (d_out,), dtype=np.float64)
+    _check(_load().oracle_out_proj(_ptr(ab), dta, _ptr(wb), _ptr(bb), dtw, _ptr(y), M, d_in, d_out),
+           "out_proj")
+    return y
+
+
+def layer_attn_out(x, W, bias, Wo, bo, H, causal=False, kv_len=None):
+    """layer_attn followed by the output projection (d -> d): [B,S,d]."""
+    ts = [x, W, Wo] + ([] if bias is None else [bias]) + ([] if bo is None else [bo])
+    _, dt = _same_type(*ts)
+    xb, wb, wob = (_as_buffer(t)[0] for t in (x, W, Wo))
+    bb = None if bias is None else _as_buffer(bias)[0]
+    bob = None if bo is None else _as_buffer(bo)[0]
+    B, S, dm = xb.shape
+    assert wob.shape == (dm, dm)
+    kl = _kvlen(kv_len, B)
+    y = np.zeros((B, S, dm))
+    _check(_load().oracle_layer_attn_out(_ptr(xb), _ptr(wb), _ptr(bb), _ptr(wob), _ptr(bob), dt, _ptr(y),
+                                         B, S, dm, H, int(bool(causal)), _ptr(kl)), "layer_attn_out")
+    return y
 
 
 def widen(t):

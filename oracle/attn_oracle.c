@@ -27,11 +27,16 @@
  *     "Roofline", sections What it does / How we built it.
  *   - Split-KV partials merged by log-sum-exp: the same algebra as the online
  *     softmax above, applied to disjoint key ranges.
+ *   - Output projection y = o Wo + bo after the heads are merged: the
+ *     fourth d x d projection of the layer ("Shape-Aware Attention", section
+ *     How we built it: the 8BSd^2 term counts Q, K, V and output).
  *
  * Readings taken where the pages are silent:
  *   - a query row with no valid key returns a zero row;
  *   - inputs are the exact stored values (fp32, bf16 or fp16) widened to fp64;
  *     nothing is rounded inside the oracle.
+ *   - the sublayer's attention output enters the output projection
+ *     unrounded (the GPU stores it in the model's element type first).
  *
  * Every function here is pinned by tests that do not re-type its formula:
  * closed forms (Q = 0 gives the mean of V, S_kv = 1 returns v_0, two keys give
@@ -515,6 +520,50 @@ int oracle_layer_attn(const void *x, const void *W, const void *bias, int dt, do
     free(k);
     free(v);
     free(oh);
+    return rc;
+}
+
+/*
+ * Output projection of the sublayer: the fourth of the layer's d x d
+ * projections ("Shape-Aware Attention", section How we built it: the 8BSd^2
+ * term of the per-layer FLOP count covers Q, K, V and output).
+ *   y [M, d_out] = a [M, d_in] . Wo [d_in, d_out] + bo [d_out] (bo may be NULL)
+ * a has its own element type code (the sublayer below passes its fp64
+ * attention output); Wo and bo share dt_w.  y is fp64.
+ */
+int oracle_out_proj(const void *a, int dt_a, const void *W, const void *bias, int dt_w,
+                    double *y, long long M, int d_in, int d_out)
+{
+    if (M < 0 || d_in < 1 || d_out < 1) return -1;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long r = 0; r < M; ++r) {
+        for (int n = 0; n < d_out; ++n) {
+            double acc = 0.0;
+            for (int c = 0; c < d_in; ++c)
+                acc += load(a, dt_a, r * d_in + c) * load(W, dt_w, (long long)c * d_out + n);
+            if (bias) acc += load(bias, dt_w, n);
+            y[r * d_out + n] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The sublayer with its output projection: oracle_layer_attn, then
+ * oracle_out_proj (d_model -> d_model) applied to its fp64 result, which is
+ * not rounded in between.  y [B, S, d_model].
+ */
+int oracle_layer_attn_out(const void *x, const void *Wqkv, const void *bqkv,
+                          const void *Wo, const void *bo, int dt, double *y,
+                          int B, long long S, int d_model, int H, int causal,
+                          const int32_t *kv_len)
+{
+    size_t n = (size_t)B * S * d_model;
+    double *o = (double *)malloc(sizeof(double) * (n ? n : 1));
+    if (!o) return -1;
+    int rc = oracle_layer_attn(x, Wqkv, bqkv, dt, o, B, S, d_model, H, causal, kv_len);
+    if (rc == 0) rc = oracle_out_proj(o, ORC_F64, Wo, bo, dt, y, (long long)B * S, d_model, d_model);
+    free(o);
     return rc;
 }
 

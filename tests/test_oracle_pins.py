@@ -325,3 +325,77 @@ def test_layer_attn_matches_library_pipeline(causal):
     ref, _ = _sdpa64(q, k, v, causal, kv_len)
     ref = ref.transpose(0, 2, 1, 3).reshape(B, S, dm)
     assert np.allclose(o, ref, atol=1e-12, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# output projection and the sublayer with it
+# --------------------------------------------------------------------------
+def test_out_proj_cyclic_shift_moves_columns_one_way():
+    """Wo[i, (i+1) % d] = 1 sends column i of a to column i+1 of y; a transposed
+    weight would send it to column i-1."""
+    M, d = 5, 12
+    a = torch.randn(M, d, generator=torch.Generator().manual_seed(60), dtype=torch.float64)
+    W = torch.zeros(d, d, dtype=torch.float64)
+    W[torch.arange(d), (torch.arange(d) + 1) % d] = 1.0
+    bias = torch.arange(d, dtype=torch.float64)
+    y = oracle.out_proj(a, W, bias)
+    want = np.roll(a.numpy(), 1, axis=1) + bias.numpy()
+    assert np.array_equal(y, want)
+
+
+def test_out_proj_small_integers_exact_by_brute_force():
+    """Small integers: every product and sum is exact in fp64, so the result
+    must equal plain integer arithmetic bit for bit (non-square, with bias)."""
+    g = torch.Generator().manual_seed(61)
+    M, d_in, d_out = 4, 6, 5
+    a = torch.randint(-4, 5, (M, d_in), generator=g).to(torch.float32)
+    W = torch.randint(-4, 5, (d_in, d_out), generator=g).to(torch.float32)
+    b = torch.randint(-9, 10, (d_out,), generator=g).to(torch.float32)
+    y = oracle.out_proj(a, W, b)
+    ai, Wi, bi = a.int().tolist(), W.int().tolist(), b.int().tolist()
+    for r in range(M):
+        for n in range(d_out):
+            assert y[r, n] == sum(ai[r][c] * Wi[c][n] for c in range(d_in)) + bi[n]
+
+
+def test_out_proj_zero_weight_gives_bias():
+    a = torch.randn(3, 4, 8, dtype=torch.float64)
+    b = torch.linspace(-1, 1, 8, dtype=torch.float64)
+    y = oracle.out_proj(a, torch.zeros(8, 8, dtype=torch.float64), b)
+    assert y.shape == (3, 4, 8)
+    assert np.array_equal(y, np.broadcast_to(b.numpy(), (3, 4, 8)))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_out_proj_matches_matmul(dtype):
+    Wo, bo = inputs.out_proj_inputs(32, dtype=dtype, seed=62, bias="normal")
+    a = torch.randn(2, 7, 32, generator=torch.Generator().manual_seed(63)).to(dtype)
+    y = oracle.out_proj(a, Wo, bo)
+    want = _np(a).reshape(14, 32) @ _np(Wo) + _np(bo)
+    assert np.allclose(y.reshape(14, 32), want, atol=1e-12, rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_layer_attn_out_matches_library_pipeline(causal):
+    """Projection, torch float64 SDPA, head merge, then a float64 matmul with
+    Wo: the oracle's sublayer with its output projection must agree."""
+    B, S, dm, H = 2, 9, 32, 4
+    x, W, b = inputs.layer_inputs(B, S, dm, seed=64, bias="normal")
+    Wo, bo = inputs.out_proj_inputs(dm, seed=65, bias="normal")
+    kv_len = torch.tensor([9, 5], dtype=torch.int32)
+    y = oracle.layer_attn_out(x, W, b, Wo, bo, H, causal=causal, kv_len=kv_len)
+    D = dm // H
+    p = torch.from_numpy(_np(x).reshape(B * S, dm) @ _np(W) + _np(b)).reshape(B, S, 3, H, D)
+    q, k, v = (p[:, :, t].transpose(1, 2).contiguous() for t in range(3))
+    o, _ = _sdpa64(q, k, v, causal, kv_len)
+    o = o.transpose(0, 2, 1, 3).reshape(B * S, dm)
+    want = (o @ _np(Wo) + _np(bo)).reshape(B, S, dm)
+    assert np.allclose(y, want, atol=1e-12, rtol=1e-12)
+
+
+def test_layer_attn_out_identity_weight_is_layer_attn():
+    B, S, dm, H = 1, 6, 16, 2
+    x, W, b = inputs.layer_inputs(B, S, dm, seed=66, bias="normal")
+    eye = torch.eye(dm, dtype=torch.float32)
+    y = oracle.layer_attn_out(x, W, b, eye, None, H, causal=True)
+    assert np.array_equal(y, oracle.layer_attn(x, W, b, H, causal=True))
