@@ -68,7 +68,14 @@ typedef enum {
 typedef enum { LA_F32 = 0, LA_BF16 = 1, LA_F16 = 2 } la_dtype;
 
 /* Operation codes for la_workspace_size(). */
-typedef enum { LA_OP_ATTN_FWD = 0, LA_OP_ATTN_CHUNKED = 1, LA_OP_LAYER_ATTN = 2, LA_OP_QKV_PROJ = 3 } la_op;
+typedef enum {
+    LA_OP_ATTN_FWD = 0,
+    LA_OP_ATTN_CHUNKED = 1,
+    LA_OP_LAYER_ATTN = 2,
+    LA_OP_QKV_PROJ = 3,
+    LA_OP_OUT_PROJ = 4,
+    LA_OP_LAYER_ATTN_OUT = 5
+} la_op;
 
 /*
  * Growing key/value cache for the chunked mode.  k and v are caller-owned
@@ -155,7 +162,8 @@ la_status la_attn_chunked(const void *q_chunk, const void *k_chunk, const void *
  * attention per head with scale 1/sqrt(D), heads merged in the store:
  *   x [B, S, d_model], Wqkv [d_model, 3*d_model], bqkv [3*d_model] or NULL,
  *   o [B, S, d_model] with head h in columns h*D .. h*D+D-1.
- * The output projection is not applied.  ws must hold at least
+ * The output projection is not applied (la_layer_attn_out applies it).  ws
+ * must hold at least
  * la_workspace_size(LA_OP_LAYER_ATTN, B, H, S, S, d_model / H, dt) bytes
  * (the head-major q, k, v; for fp32 V is kept transposed and the weight's
  * transpose is kept too); otherwise LA_ERR_WORKSPACE.
@@ -164,6 +172,48 @@ la_status la_layer_attn(const void *x, const void *Wqkv, const void *bqkv, void 
                         int B, int S, int d_model, int H, int causal,
                         const int32_t *kv_len, la_dtype dt,
                         void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
+ * Output projection of the sublayer, the fourth of the layer's d x d
+ * projections ("Shape-Aware Attention", section How we built it: the 8BSd^2
+ * term of the per-layer FLOP count covers the Q, K, V and output
+ * projections):
+ *   y [M, d_model] = a [M, d_model] . Wo [d_model, d_model] + bo
+ *   a   row-major activations (for the sublayer: the heads-merged attention
+ *       output, M = B*S)
+ *   Wo  [d_model, d_model] row-major (input features are rows)
+ *   bo  [d_model] or NULL
+ * d_model must be a positive multiple of 64 (else LA_ERR_UNSUPPORTED); M >= 0
+ * (M == 0 is a no-op).  fp32 runs the products in TF32 like the other
+ * projections.  ws, ws_bytes: la_workspace_size(LA_OP_OUT_PROJ, 1, H, M, M,
+ * D, dt) bytes for any H, D with H*D = d_model; fp32 needs
+ * d_model*d_model*4 bytes there (Wo is transposed into it first; TF32
+ * products take K-major operands only), bf16/fp16 none (ws may be NULL).
+ * a and y must not overlap.
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE or
+ * LA_ERR_CUDA.
+ */
+la_status la_out_proj(const void *a, const void *Wo, const void *bo, void *y,
+                      int M, int d_model, la_dtype dt,
+                      void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
+ * The sublayer with its output projection: la_layer_attn, then la_out_proj
+ * on its heads-merged output, which is stored in the element type dt in
+ * between (as a separate la_out_proj call would see it):
+ *   x [B, S, d_model], Wqkv [d_model, 3*d_model], bqkv [3*d_model] or NULL,
+ *   Wo [d_model, d_model], bo [d_model] or NULL,
+ *   y [B, S, d_model] = merge_heads(attention) . Wo + bo.
+ * Arguments otherwise as for la_layer_attn.  ws must hold at least
+ * la_workspace_size(LA_OP_LAYER_ATTN_OUT, B, H, S, S, d_model / H, dt)
+ * bytes (the intermediate output, the fp32 weight transposes and the
+ * sublayer's own workspace); otherwise LA_ERR_WORKSPACE.
+ */
+la_status la_layer_attn_out(const void *x, const void *Wqkv, const void *bqkv,
+                            const void *Wo, const void *bo, void *y,
+                            int B, int S, int d_model, int H, int causal,
+                            const int32_t *kv_len, la_dtype dt,
+                            void *ws, size_t ws_bytes, la_stream_t st);
 
 /*
  * la_attn_fwd without a workspace, for callers that cannot allocate device
@@ -199,9 +249,10 @@ la_status la_attn_fwd_noalloc(const void *q, const void *k, const void *v, void 
 /*
  * Workspace bytes an operation wants (0 if none).  op is an la_op; the
  * remaining arguments are those of the call (for LA_OP_ATTN_CHUNKED pass
- * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN and
- * LA_OP_QKV_PROJ pass S_q = S_kv = S and D = d_model / H).  Returns (size_t)-1 for invalid arguments.  Host only;
- * touches no device.
+ * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN,
+ * LA_OP_LAYER_ATTN_OUT and LA_OP_QKV_PROJ pass S_q = S_kv = S and
+ * D = d_model / H; for LA_OP_OUT_PROJ see la_out_proj).  Returns (size_t)-1
+ * for invalid arguments.  Host only; touches no device.
  */
 size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt);
 

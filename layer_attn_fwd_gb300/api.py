@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "liblayerattn.so")
 
 LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_INTERNAL = range(7)
 LA_F32, LA_BF16, LA_F16 = 0, 1, 2
-LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN, LA_OP_QKV_PROJ = 0, 1, 2, 3
+LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN, LA_OP_QKV_PROJ, LA_OP_OUT_PROJ, LA_OP_LAYER_ATTN_OUT = range(6)
 
 _DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16, torch.float16: LA_F16}
 
@@ -57,6 +57,8 @@ def load(path: str | None = None):
         lib.la_attn_fwd_noalloc.restype = I
         lib.la_attn_chunked.argtypes = [P, P, P, ctypes.POINTER(la_kv_cache), P, I, I, F, P, Z, P]
         lib.la_layer_attn.argtypes = [P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
+        lib.la_out_proj.argtypes = [P, P, P, P, I, I, I, P, Z, P]
+        lib.la_layer_attn_out.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
         lib.la_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.la_workspace_size.restype = Z
         lib.la_get_last_error.argtypes = [P]
@@ -66,7 +68,8 @@ def load(path: str | None = None):
         lib.la_debug_inject_timeout.restype = I
         lib.la_status_string.argtypes = [I]
         lib.la_status_string.restype = ctypes.c_char_p
-        for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_get_last_error"):
+        for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_out_proj",
+                     "la_layer_attn_out", "la_get_last_error"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -231,6 +234,38 @@ def layer_attn(x, Wqkv, bqkv, H, causal=False, kv_len=None, out=None, workspace=
     _check(load().la_layer_attn(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(o), B, S, dm, H, int(bool(causal)),
                                 _ptr(kv_len), _dt(x), _ptr(workspace), nbytes, _stream(stream)), "la_layer_attn")
     return o
+
+
+def out_proj(a, Wo, bo=None, out=None, workspace=None, stream=None):
+    """a [..., d] (row-major), Wo [d, d], bo [d] or None -> a Wo + bo."""
+    for t, n in ((a, "a"), (Wo, "Wo")):
+        _need(t, n)
+    if bo is not None:
+        _need(bo, "bo")
+    dm = a.shape[-1]
+    M = a.numel() // dm if dm > 0 else 0
+    y = torch.empty_like(a) if out is None else out
+    if workspace is None and dm % 64 == 0 and dm > 0 and a.dtype in _DT:
+        workspace = _workspace(workspace_size(LA_OP_OUT_PROJ, 1, dm // 64, M, M, 64, a.dtype), a.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_out_proj(_ptr(a), _ptr(Wo), _ptr(bo), _ptr(y), M, dm, _dt(a), _ptr(workspace), nbytes,
+                              _stream(stream)), "la_out_proj")
+    return y
+
+
+def layer_attn_out(x, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=None, out=None, workspace=None, stream=None):
+    """The sublayer with its output projection: x [B,S,d] -> [B,S,d]."""
+    _need(x, "x")
+    B, S, dm = x.shape
+    D = dm // H if H > 0 else 0
+    y = torch.empty_like(x) if out is None else out
+    if workspace is None:
+        workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN_OUT, B, H, S, S, D, x.dtype), x.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_layer_attn_out(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), _ptr(y), B, S, dm, H,
+                                    int(bool(causal)), _ptr(kv_len), _dt(x), _ptr(workspace), nbytes,
+                                    _stream(stream)), "la_layer_attn_out")
+    return y
 
 
 def last_error_detail() -> int:

@@ -156,6 +156,11 @@ size_t wt_bytes(la_dtype dt, int d_model) {
   if (dt != LA_F32) return 0;
   return round_up(static_cast<size_t>(3) * d_model * d_model * 4, 256);
 }
+// fp32 only: Wo^T [d, d] for the TF32 output projection.
+size_t wot_bytes(la_dtype dt, int d_model) {
+  if (dt != LA_F32) return 0;
+  return round_up(static_cast<size_t>(d_model) * d_model * 4, 256);
+}
 
 // Split the key range only when the unsplit grid leaves the GPU short of
 // full waves; estimate makespan as waves x tiles per CTA (+2 tiles of fixed
@@ -318,15 +323,16 @@ la_status check_proj_args(const void* x, const void* W, const void* bias, const 
   return LA_OK;
 }
 
-// Projection; scratch from ws: the fp32 Wqkv^T.  With vt != nullptr (fp32
-// sublayer) V is written as V^T [B, H, D, vt_ld] there instead of into v.
+// Projection; scratch from ws: the fp32 Wqkv^T (transposed there first,
+// unless wt_ready says it already is).  With vt != nullptr (fp32 sublayer) V
+// is written as V^T [B, H, D, vt_ld] there instead of into v.
 la_status run_proj(const void* x, const void* W, const void* bias, void* q, void* k, void* v, int B, int S,
-                   int d_model, int H, float q_scale, la_dtype dt, void* ws, size_t ws_bytes, void* vt,
-                   long long vt_ld, cudaStream_t st) {
+                   int d_model, int H, float q_scale, la_dtype dt, void* ws, size_t ws_bytes, bool wt_ready,
+                   void* vt, long long vt_ld, cudaStream_t st) {
   const long long M = static_cast<long long>(B) * S;
   if (M == 0) return LA_OK;
   ProjShape ps;
-  if (!proj_shape(dt, &ps)) return LA_ERR_UNSUPPORTED;
+  if (!proj_shape(dt, M, 3LL * d_model, device_sms(), &ps)) return LA_ERR_UNSUPPORTED;
   uint32_t* err = error_word();
   if (err == nullptr) return LA_ERR_CUDA;
   CUtensorMap tx, tw;
@@ -335,7 +341,8 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   if (ps.w_transposed) {
     const size_t need = wt_bytes(dt, d_model);
     if (ws == nullptr || ws_bytes < need) return LA_ERR_WORKSPACE;
-    if (launch_transpose32(W, 0, ws, d_model, 1, d_model, 3 * d_model, st) != cudaSuccess) return LA_ERR_CUDA;
+    if (!wt_ready && launch_transpose32(W, 0, ws, d_model, 1, d_model, 3 * d_model, st) != cudaSuccess)
+      return LA_ERR_CUDA;
     s = map_2d(&tw, ws, dt, 3LL * d_model, d_model, ps.block_n, ps.box_cols);
   } else {
     s = map_2d(&tw, W, dt, d_model, 3LL * d_model, ps.box_k_rows, ps.box_cols);
@@ -357,11 +364,100 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   a.err = err;
   a.v_transposed = vt != nullptr;
   a.S_pad = vt_ld;
-  return cuda_status(launch_proj(dt, tx, tw, a, st));
+  return cuda_status(launch_proj(dt, ps.block_n, tx, tw, a, st));
+}
+
+// Output projection y [M, d] = a [M, d] . Wo [d, d] + bo on the projection
+// GEMM: a row-major output is its head-major case with one batch entry and
+// one head as wide as the row.  fp32 reads Wo^T [d, d] from wot, transposed
+// there beforehand (TF32 products take K-major operands only).
+la_status run_out_proj(const void* a_in, const void* Wo, const void* wot, const void* bo, void* y, long long M,
+                       int d, la_dtype dt, cudaStream_t st) {
+  if (M == 0) return LA_OK;
+  ProjShape ps;
+  if (!proj_shape(dt, M, d, device_sms(), &ps)) return LA_ERR_UNSUPPORTED;
+  uint32_t* err = error_word();
+  if (err == nullptr) return LA_ERR_CUDA;
+  CUtensorMap tx, tw;
+  la_status s = map_2d(&tx, a_in, dt, M, d, kTileM, ps.box_cols);
+  if (s != LA_OK) return s;
+  if (ps.w_transposed)
+    s = map_2d(&tw, wot, dt, d, d, ps.block_n, ps.box_cols);
+  else
+    s = map_2d(&tw, Wo, dt, d, d, ps.box_k_rows, ps.box_cols);
+  if (s != LA_OK) return s;
+  ProjArgs a;
+  memset(&a, 0, sizeof a);
+  a.bias = bo;
+  a.q = a.k = a.v = y;  // N == K: every column is in the first block
+  a.M = static_cast<int>(M);
+  a.N = d;
+  a.K = d;
+  a.S = static_cast<int>(M);
+  a.H = 1;
+  a.D = d;
+  a.q_scale = 1.f;
+  a.err = err;
+  return cuda_status(launch_proj(dt, ps.block_n, tx, tw, a, st));
+}
+
+la_status check_out_proj_args(const void* a_in, const void* Wo, const void* bo, const void* y, long long M,
+                              int d_model, int dt) {
+  if (!a_in || !Wo || !y) return LA_ERR_INVALID;
+  if (M < 0 || d_model < 1 || !dtype_ok(dt)) return LA_ERR_INVALID;
+  if (d_model % 64 != 0) return LA_ERR_UNSUPPORTED;
+  if (M > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+  if (!aligned16(a_in) || !aligned16(Wo) || !aligned16(y)) return LA_ERR_INVALID;
+  if (bo != nullptr && (reinterpret_cast<uintptr_t>(bo) & 3u)) return LA_ERR_INVALID;
+  return LA_OK;
 }
 
 size_t layer_qkv_bytes(int B, int S, int d_model, la_dtype dt) {
   return round_up(static_cast<size_t>(B) * S * d_model * elem_bytes(dt), 256);
+}
+
+size_t layer_fixed_bytes(int B, int S, int d_model, int H, la_dtype dt) {
+  const size_t one = layer_qkv_bytes(B, S, d_model, dt);
+  const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S, d_model / H) : one;
+  return 2 * one + vbytes + wt_bytes(dt, d_model);
+}
+
+// The sublayer without its output projection: ws holds q | k | v (fp32: V^T
+// [B,H,D,S_pad]) | fp32 Wqkv^T | split partials.  With wt_ready the fp32
+// Wqkv^T is already in place.
+la_status run_layer(const void* x, const void* Wqkv, const void* bqkv, void* o, int B, int S, int d_model, int H,
+                    int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes, bool wt_ready,
+                    cudaStream_t cs) {
+  const int D = d_model / H;
+  const size_t one = layer_qkv_bytes(B, S, d_model, dt);
+  const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S, D) : one;
+  const size_t fixed = layer_fixed_bytes(B, S, d_model, H, dt);
+  if (ws_bytes < fixed) return LA_ERR_WORKSPACE;
+  if (S == 0) return LA_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void *q = w, *k = w + one, *v = w + 2 * one;
+  uint8_t* wt = w + 2 * one + vbytes;
+  const bool vt = dt == LA_F32;
+  la_status s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, wt, wt_bytes(dt, d_model), wt_ready,
+                         vt ? v : nullptr, vt_pad(S), cs);
+  if (s != LA_OK) return s;
+  const float scale = 1.0f / sqrtf(static_cast<float>(D));
+  const KVView kv{k, v, S, vt ? v : nullptr, vt_pad(S)};
+  return run_attention(q, kv, o, static_cast<long long>(S) * d_model, D, d_model, B, H, S, S, D, causal, scale,
+                       kv_len, dt, w + fixed, ws_bytes - fixed, cs);
+}
+
+la_status check_layer_args(const void* x, const void* Wqkv, const void* bqkv, const void* o, const void* ws, int B,
+                           int S, int d_model, int H, const int32_t* kv_len, int dt) {
+  if (!o || !ws) return LA_ERR_INVALID;
+  if (!aligned16(o) || !aligned16(ws)) return LA_ERR_INVALID;
+  // validate with placeholders for the q/k/v pointers, which live in ws
+  la_status s = check_proj_args(x, Wqkv, bqkv, ws, ws, ws, B, S, d_model, H, 1.f, dt);
+  if (s != LA_OK) return s;
+  s = check_attn_args(B, H, S, S, d_model / H, 1.f, dt);
+  if (s != LA_OK) return s;
+  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return LA_ERR_INVALID;
+  return LA_OK;
 }
 
 }  // namespace
@@ -377,7 +473,7 @@ la_status la_qkv_proj(const void* x, const void* Wqkv, const void* bqkv, void* q
   if (s != LA_OK) return s;
   if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
   if (S > 0 && (ws == nullptr ? 0 : ws_bytes) < wt_bytes(dt, d_model)) return LA_ERR_WORKSPACE;
-  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, ws, ws_bytes, nullptr, 0,
+  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, ws, ws_bytes, false, nullptr, 0,
                   reinterpret_cast<cudaStream_t>(st));
 }
 
@@ -431,33 +527,54 @@ la_status la_attn_chunked(const void* q_chunk, const void* k_chunk, const void* 
 la_status la_layer_attn(const void* x, const void* Wqkv, const void* bqkv, void* o, int B, int S, int d_model,
                         int H, int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes,
                         la_stream_t st) {
-  if (!o || !ws) return LA_ERR_INVALID;
-  if (!aligned16(o) || !aligned16(ws)) return LA_ERR_INVALID;
-  // validate with placeholders for the q/k/v pointers, which live in ws
-  la_status s = check_proj_args(x, Wqkv, bqkv, ws, ws, ws, B, S, d_model, H, 1.f, dt);
+  la_status s = check_layer_args(x, Wqkv, bqkv, o, ws, B, S, d_model, H, kv_len, dt);
   if (s != LA_OK) return s;
-  const int D = d_model / H;
-  s = check_attn_args(B, H, S, S, D, 1.f, dt);
+  return run_layer(x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, ws, ws_bytes, false,
+                   reinterpret_cast<cudaStream_t>(st));
+}
+
+la_status la_out_proj(const void* a, const void* Wo, const void* bo, void* y, int M, int d_model, la_dtype dt,
+                      void* ws, size_t ws_bytes, la_stream_t st) {
+  la_status s = check_out_proj_args(a, Wo, bo, y, M, d_model, dt);
   if (s != LA_OK) return s;
-  if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return LA_ERR_INVALID;
-  // ws: q | k | v (fp32: V^T [B,H,D,S_pad]) | fp32 Wqkv^T | split partials
-  const size_t one = layer_qkv_bytes(B, S, d_model, dt);
-  const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S, D) : one;
-  const size_t fixed = 2 * one + vbytes + wt_bytes(dt, d_model);
-  if (ws_bytes < fixed) return LA_ERR_WORKSPACE;
+  if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
+  if (M == 0) return LA_OK;
+  if ((ws == nullptr ? 0 : ws_bytes) < wot_bytes(dt, d_model)) return LA_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
+  if (dt == LA_F32 && launch_transpose32(Wo, 0, ws, d_model, 1, d_model, d_model, cs) != cudaSuccess)
+    return LA_ERR_CUDA;
+  return run_out_proj(a, Wo, ws, bo, y, M, d_model, dt, cs);
+}
+
+la_status la_layer_attn_out(const void* x, const void* Wqkv, const void* bqkv, const void* Wo, const void* bo,
+                            void* y, int B, int S, int d_model, int H, int causal, const int32_t* kv_len,
+                            la_dtype dt, void* ws, size_t ws_bytes, la_stream_t st) {
+  la_status s = check_layer_args(x, Wqkv, bqkv, y, ws, B, S, d_model, H, kv_len, dt);
+  if (s != LA_OK) return s;
+  s = check_out_proj_args(ws, Wo, bo, y, static_cast<long long>(B) * S, d_model, dt);
+  if (s != LA_OK) return s;
+  // ws: heads-merged attention output o [B,S,d] | fp32 Wo^T | the sublayer's own workspace
+  const size_t obytes = layer_qkv_bytes(B, S, d_model, dt);
+  const size_t wob = wot_bytes(dt, d_model);
+  if (ws_bytes < obytes + wob + layer_fixed_bytes(B, S, d_model, H, dt)) return LA_ERR_WORKSPACE;
   if (S == 0) return LA_OK;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void *q = w, *k = w + one, *v = w + 2 * one;
-  uint8_t* wt = w + 2 * one + vbytes;
+  void* o = w;
+  void* wot = w + obytes;
+  uint8_t* lw = w + obytes + wob;
+  const size_t lw_bytes = ws_bytes - obytes - wob;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
-  const bool vt = dt == LA_F32;
-  s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, wt, wt_bytes(dt, d_model), vt ? v : nullptr,
-               vt_pad(S), cs);
+  if (dt == LA_F32) {
+    // both weight transposes first: Wqkv^T (an ordinary launch, so everything
+    // before this call has finished), then Wo^T, which may overlap it
+    const size_t one = layer_qkv_bytes(B, S, d_model, dt);
+    uint8_t* wt = lw + 2 * one + vt_bytes(dt, B, H, S, d_model / H);
+    if (launch_transpose32(Wqkv, 0, wt, d_model, 1, d_model, 3 * d_model, cs) != cudaSuccess) return LA_ERR_CUDA;
+    if (launch_transpose32(Wo, 0, wot, d_model, 1, d_model, d_model, cs, true) != cudaSuccess) return LA_ERR_CUDA;
+  }
+  s = run_layer(x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, lw, lw_bytes, dt == LA_F32, cs);
   if (s != LA_OK) return s;
-  const float scale = 1.0f / sqrtf(static_cast<float>(D));
-  const KVView kv{k, v, S, vt ? v : nullptr, vt_pad(S)};
-  return run_attention(q, kv, o, static_cast<long long>(S) * d_model, D, d_model, B, H, S, S, D, causal, scale,
-                       kv_len, dt, w + fixed, ws_bytes - fixed, cs);
+  return run_out_proj(o, Wo, wot, bo, y, static_cast<long long>(B) * S, d_model, dt, cs);
 }
 
 size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt) {
@@ -469,12 +586,18 @@ size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtyp
       return attn_ws_bytes(dt, B, H, S_q, S_kv, D, true);
     case LA_OP_LAYER_ATTN: {
       if (S_q != S_kv) return bad;
-      const size_t one = layer_qkv_bytes(B, S_q, H * D, dt);
-      const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S_q, D) : one;
-      return 2 * one + vbytes + wt_bytes(dt, H * D) + attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);
+      return layer_fixed_bytes(B, S_q, H * D, H, dt) + attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);
     }
     case LA_OP_QKV_PROJ:
       return wt_bytes(dt, H * D);
+    case LA_OP_OUT_PROJ:
+      return wot_bytes(dt, H * D);
+    case LA_OP_LAYER_ATTN_OUT: {
+      if (S_q != S_kv) return bad;
+      const int dm = H * D;
+      return layer_qkv_bytes(B, S_q, dm, dt) + wot_bytes(dt, dm) + layer_fixed_bytes(B, S_q, dm, H, dt) +
+             attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);
+    }
     default:
       return bad;
   }

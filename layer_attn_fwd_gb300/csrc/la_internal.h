@@ -83,9 +83,12 @@ cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st);
 
 // Batched transpose of 4-byte elements: dst[b][c][r] = src[b][r][c]; source
 // rows of C elements, batches src_batch apart; destination rows of ld_dst
-// elements, batches C*ld_dst apart.
+// elements, batches C*ld_dst apart.  pdl: launch with programmatic stream
+// serialization, so that it may overlap the previous grid (it must touch
+// nothing that grid writes; it waits for that grid before it exits, so the
+// grids after it still see everything before it finished).
 cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
-                               int R, int C, cudaStream_t st);
+                               int R, int C, cudaStream_t st, bool pdl = false);
 
 // Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`.
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
@@ -97,7 +100,7 @@ struct ProjArgs {
   void* q;
   void* k;
   void* v;
-  int M, N, K;        // rows (B*S), 3*d_model, d_model
+  int M, N, K;        // rows (B*S), output columns (3*d_model), d_model
   int S, H, D;
   float q_scale;
   uint32_t* err;
@@ -105,13 +108,17 @@ struct ProjArgs {
   long long S_pad;    // row length of V^T
 };
 struct ProjShape {
-  int block_n;        // output columns per CTA
+  int block_n;        // output columns per tile (the wide tile or 128)
   int box_cols;       // TMA box columns (one 128-byte swizzle row)
   int box_k_rows;     // TMA box rows of the weight tile (= K per stage)
   bool w_transposed;  // the weight is read as Wqkv^T [3d, d] (TF32: K-major only)
 };
-bool proj_shape(la_dtype dt, ProjShape* s);
-cudaError_t launch_proj(la_dtype dt, const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a,
+// Shape of a projection launch over an M x N output on `sms` SMs.
+bool proj_shape(la_dtype dt, long long M, long long N, int sms, ProjShape* s);
+// The persistent projection GEMM.  A row-major [M, N] output is the
+// head-major case with one batch entry (S = M), one head (H = 1, D = N) and
+// N <= K, so that every column belongs to the q block.
+cudaError_t launch_proj(la_dtype dt, int block_n, const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a,
                         cudaStream_t st);
 
 }  // namespace la

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(256)
       if (r + 3 < R) p[3] = w3;
     }
   }
+  // Under programmatic serialization this grid may run beside the one before
+  // it; waiting for that grid before exiting keeps the stream's order for the
+  // grids after this one.  A no-op for an ordinary launch.
+  pdl_wait();
 }
 
 int sm_count() {
@@ -197,15 +201,17 @@ cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
-                               int R, int C, cudaStream_t st) {
+                               int R, int C, cudaStream_t st, bool pdl) {
   if (batches == 0 || R == 0 || C == 0) return cudaSuccess;
   if (batches > 65535 || (C + 63) / 64 > 65535) return cudaErrorInvalidValue;
   const long long dst_batch = static_cast<long long>(C) * ld_dst;
   const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
                   C % 4 == 0 && ld_dst % 4 == 0 && src_batch % 4 == 0 && dst_batch % 4 == 0;
   dim3 grid((R + 63) / 64, (C + 63) / 64, static_cast<unsigned>(batches));
-  transpose32_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(src), reinterpret_cast<uint32_t*>(dst), R,
-                                            C, ld_dst, src_batch, dst_batch, vec);
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
+  uint32_t* d = reinterpret_cast<uint32_t*>(dst);
+  if (pdl) return launch_pdl(transpose32_kernel, grid, dim3(256), 0, st, s, d, R, C, ld_dst, src_batch, dst_batch, vec);
+  transpose32_kernel<<<grid, 256, 0, st>>>(s, d, R, C, ld_dst, src_batch, dst_batch, vec);
   return cudaGetLastError();
 }
 

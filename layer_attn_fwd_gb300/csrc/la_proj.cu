@@ -8,7 +8,11 @@
 // buffered, so the epilogue of one tile (bias, Q scale, split into heads)
 // runs while the next tile's products are issued.  The epilogue scatters the
 // tile straight into the head-major q, k, v [B, H, S, D] outputs, so the
-// split into heads costs no extra pass.
+// split into heads costs no extra pass.  The same kernel computes the
+// sublayer's output projection y = o.Wo + bo: a row-major [M, d] output is the
+// head-major layout with one batch entry and one head as wide as the row.
+// Tiles are 128 rows by BNP columns, BNP the wide width or 128 (chosen per
+// launch for the fewest waves).
 //
 //   warp 4        TMA: x tile (K-major) and weight tile through an NSP-stage
 //                 ring.  bf16/fp16 read Wqkv itself (rows = K, columns = N:
@@ -358,22 +362,37 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArg
 
 }  // namespace
 
-bool proj_shape(la_dtype dt, ProjShape* s) {
+// Tile width: the wide tile (fp32 192, half 256 columns) unless the
+// 128-column tile finishes sooner.  A tile's time grows with the bytes its
+// k-steps move through shared memory (the 128-row x tile plus the block_n-row
+// weight tile), so a launch costs about waves x (128 + block_n); ties keep the
+// wide tile.  Every tile shape gives the same result.
+bool proj_shape(la_dtype dt, long long M, long long N, int sms, ProjShape* s) {
   if (dt != LA_F32 && dt != LA_BF16 && dt != LA_F16) return false;
   const int e = dt == LA_F32 ? 4 : 2;
-  s->block_n = dt == LA_F32 ? 192 : 256;
+  const int wide = dt == LA_F32 ? 192 : 256;
+  const long long m_tiles = (M + kTileM - 1) / kTileM;
+  auto cost = [&](int bn) {
+    const long long tiles = m_tiles * ((N + bn - 1) / bn);
+    const long long waves = (tiles + sms - 1) / (sms > 0 ? sms : 1);
+    return waves * (kTileM + bn);
+  };
+  s->block_n = cost(128) < cost(wide) ? 128 : wide;
   s->box_cols = 128 / e;
   s->box_k_rows = 128 / e;
   s->w_transposed = (dt == LA_F32);
   return true;
 }
 
-cudaError_t launch_proj(la_dtype dt, const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a,
+cudaError_t launch_proj(la_dtype dt, int block_n, const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a,
                         cudaStream_t st) {
+  const bool narrow = block_n == 128;
+  if (!narrow && block_n != (dt == LA_F32 ? 192 : 256)) return cudaErrorInvalidValue;
   switch (dt) {
-    case LA_BF16: return launch_p<__nv_bfloat16, 256, 4>(tx, tw, a, st);
-    case LA_F16: return launch_p<__half, 256, 4>(tx, tw, a, st);
-    case LA_F32: return launch_p<float, 192, 5>(tx, tw, a, st);
+    case LA_BF16:
+      return narrow ? launch_p<__nv_bfloat16, 128, 6>(tx, tw, a, st) : launch_p<__nv_bfloat16, 256, 4>(tx, tw, a, st);
+    case LA_F16: return narrow ? launch_p<__half, 128, 6>(tx, tw, a, st) : launch_p<__half, 256, 4>(tx, tw, a, st);
+    case LA_F32: return narrow ? launch_p<float, 128, 6>(tx, tw, a, st) : launch_p<float, 192, 5>(tx, tw, a, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -44,6 +44,11 @@ def proj_flops(B, S, d_model):
     return 2 * B * S * d_model * 3 * d_model
 
 
+def out_proj_flops(B, S, d_model):
+    """The output projection y = o Wo + bo, Wo [d, d]."""
+    return 2 * B * S * d_model * d_model
+
+
 def attn_min_bytes(B, H, S_q, S_kv, D, in_bytes, out_bytes):
     """Compulsory HBM traffic: read q, k, v once, write o once."""
     return B * H * D * (S_q * in_bytes + 2 * S_kv * in_bytes + S_q * out_bytes)

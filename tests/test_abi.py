@@ -126,3 +126,38 @@ def test_workspace_sizes(lib):
     # one long row range on a small grid splits, and asks for room for it
     n = lib.la_workspace_size(api.LA_OP_ATTN_FWD, 1, 1, 256, 8192, 128, api.LA_BF16)
     assert n >= 2 * 256 * 128 * 4
+
+
+def test_out_proj_rejects_bad_arguments(lib):
+    def call(a=FAKE, W=FAKE, b=None, y=FAKE, M=64, dm=512, dt=api.LA_BF16, ws=None, nb=0):
+        return lib.la_out_proj(a, W, b, y, M, dm, dt, ws, nb, None)
+    assert call(a=None) == api.LA_ERR_INVALID
+    assert call(y=None) == api.LA_ERR_INVALID
+    assert call(M=-1) == api.LA_ERR_INVALID
+    assert call(dm=0) == api.LA_ERR_INVALID
+    assert call(dt=5) == api.LA_ERR_INVALID
+    assert call(dm=96) == api.LA_ERR_UNSUPPORTED           # not a multiple of 64
+    assert call(a=ctypes.c_void_p(0x7f0000000004)) == api.LA_ERR_INVALID
+    assert call(b=ctypes.c_void_p(0x7f0000000002)) == api.LA_ERR_INVALID
+    assert call(dt=api.LA_F32) == api.LA_ERR_WORKSPACE     # fp32 transposes Wo into ws
+    assert call(dt=api.LA_F32, ws=FAKE, nb=512 * 512 * 4 - 1) == api.LA_ERR_WORKSPACE
+    assert call(M=0, dt=api.LA_F32) == api.LA_OK           # empty: nothing to do, nothing launched
+
+
+def test_layer_attn_out_checks_workspace_before_launch(lib):
+    need = api.workspace_size(api.LA_OP_LAYER_ATTN_OUT, 8, 8, 512, 512, 64, api.torch.float32)
+    base = api.workspace_size(api.LA_OP_LAYER_ATTN, 8, 8, 512, 512, 64, api.torch.float32)
+    assert need == base + 8 * 512 * 512 * 4 + 512 * 512 * 4     # + merged output + Wo^T
+    def call(ws=FAKE, nb=need - 1, Wo=FAKE):
+        return lib.la_layer_attn_out(FAKE, FAKE, None, Wo, None, FAKE, 8, 512, 512, 8, 0, None, api.LA_F32, ws, nb,
+                                     None)
+    assert call() == api.LA_ERR_WORKSPACE
+    assert call(ws=None, nb=need) == api.LA_ERR_INVALID
+    assert call(Wo=None, nb=need) == api.LA_ERR_INVALID
+
+
+def test_out_proj_workspace_sizes(lib):
+    assert lib.la_workspace_size(api.LA_OP_OUT_PROJ, 1, 8, 4096, 4096, 64, api.LA_F32) == 512 * 512 * 4
+    assert lib.la_workspace_size(api.LA_OP_OUT_PROJ, 1, 8, 4096, 4096, 64, api.LA_BF16) == 0
+    bf = lib.la_workspace_size(api.LA_OP_LAYER_ATTN_OUT, 8, 8, 512, 512, 64, api.LA_BF16)
+    assert bf == lib.la_workspace_size(api.LA_OP_LAYER_ATTN, 8, 8, 512, 512, 64, api.LA_BF16) + 8 * 512 * 512 * 2
