@@ -9,8 +9,9 @@ reports, each timed the same way, the other workloads of the path: fp32
 causal attention B=8 H=8 S=2048 D=64 (with and without key padding), bf16
 causal attention B=4 H=16 S=4096 D=128, the chunked 100k-token mode (bf16
 causal B=2 H=16 S=100000 D=64, windows of 4096 against a growing cache), the
-small fp32 case B=1 H=2 S=128 D=64, and the sublayer with its output
-projection (fp32 and bf16, B=8 S=512 d_model=512).
+small fp32 case B=1 H=2 S=128 D=64 (also per-call latency, direct against
+CUDA-graph replay), and the sublayer with its output projection (fp32 and
+bf16, B=8 S=512 d_model=512).
 
 FLOPs are algorithmic (useful work only): 2*rows*d*3d for the projection,
 2*rows*d*d for the output projection and 4*D per (query, visible key) pair
@@ -372,6 +373,46 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
                                   "note": "fp32 includes the Wo^T pre-pass" if dt == torch.float32 else ""}}
         del x, Wq, bq, Wo, bo, y, ws, o, wo_ws
 
+    def small_latency(key, name):
+        """Small-shape latency: back-to-back calls, host wall clock per call
+        (argument checks, tensor-map encoding and launches included), direct
+        calls against replays of the same call captured in a CUDA graph."""
+        if not wanted(key):
+            return
+        B, H, S, D = 1, 2, 128, 64
+        q, k, v = (t.to(dev) for t in inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=0))
+        o = torch.empty_like(q)
+        ws = torch.empty(api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, torch.float32), dtype=torch.uint8,
+                         device=dev)
+
+        def direct():
+            api.attn_fwd(q, k, v, out=o, workspace=ws, stream=stream)
+
+        g = api.Graph(lambda: api.attn_fwd(q, k, v, out=o, workspace=ws), stream=stream)
+
+        def replay():
+            with torch.cuda.stream(stream):
+                g.replay()
+
+        def per_call_us(fn, n=500):
+            for _ in range(50):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) / n * 1e6
+
+        us_direct, us_graph = per_call_us(direct), per_call_us(replay)
+        fl = flops.attn_flops(B, H, S, S, D, False)
+        res[name] = {"direct_us_per_call": round(us_direct, 2), "graph_us_per_call": round(us_graph, 2),
+                     "graph_speedup": round(us_direct / us_graph, 3),
+                     "graph_tflops": round(fl / (us_graph * 1e-6) / 1e12, 3), "gflop": round(fl / 1e9, 5),
+                     "launches_per_call": 2,
+                     "note": "500 back-to-back calls, inputs L2-resident (0.26 MB), no flush"}
+
+    small_latency("small-graph", "fp32 B1 H2 S128 D64 non-causal, per-call latency: direct vs CUDA-graph replay")
     layer_out_case("layer-out-fp32", "sublayer + output projection fp32 B8 S512 d512 H8 non-causal", torch.float32)
     layer_out_case("layer-out-bf16", "sublayer + output projection bf16 B8 S512 d512 H8 non-causal", torch.bfloat16)
     if not wanted("chunked-100k"):
@@ -478,7 +519,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--only", choices=["fp32-causal-2048", "fp32-causal-2048-padded", "bf16-causal-4096",
-                                       "fp32-small", "layer-out-fp32", "layer-out-bf16", "chunked-100k"],
+                                       "fp32-small", "small-graph", "layer-out-fp32", "layer-out-bf16",
+                                       "chunked-100k"],
                     help="time one named attention workload alone and print its figures (no contract line)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

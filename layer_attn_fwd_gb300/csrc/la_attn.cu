@@ -285,10 +285,10 @@ __device__ __forceinline__ int sel(const int (&je)[NQ], int t) {
 // from a global ticket counter (heaviest first, whichever CTA is free next),
 // ticket t meaning item gridDim.x + t.  Barrier phases and the key/value
 // ring continue from one item to the next, so an item's loads are issued
-// while the previous item finishes.  Ticket t of a launch is *a.sched -
-// a.sched_base; every CTA draws until it gets one past the last item, so a
-// launch draws exactly as many tickets as it has items (the host advances
-// the base by that much).
+// while the previous item finishes.  Tickets are counted from zero in
+// a.sched[0]; every CTA draws until it gets one past the last item, then
+// counts itself done in a.sched[1], and the last CTA done resets both, so
+// every launch (or CUDA-graph replay) finds them at zero.
 template <typename T, int D, int NQ, int BN, int NS, int EMU, bool PERS>
 __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -363,6 +363,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
   // The set-up above overlaps the previous grid; nothing before the wait
   // reads or writes global memory the previous grid may touch.  The tensor
   // maps are kernel parameters, so their descriptors are fetched meanwhile.
+  // The next grid may be scheduled now: its CTAs take SMs as this grid's
+  // retire and wait for all of it before touching memory.
+  if (threadIdx.x == 0) pdl_trigger();
   if (warp == C::WARP_TMA && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
       // is drawn and the launcher reserves none)
       auto draw = [&]() -> int {
         if (!PERS || n_items <= G || a.sched == nullptr) return -1;
-        const unsigned long long tk = atomicAdd(a.sched, 1ull) - a.sched_base;
+        const unsigned long long tk = atomicAdd(a.sched, 1ull);
         return tk < static_cast<unsigned long long>(n_items - G) ? G + static_cast<int>(tk) : -1;
       };
       int it = 0, na = 0, nr = 0;  // key tiles, active items and ring slots so far
@@ -479,10 +482,21 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         ++na;
       }
       // a CTA that stopped early still draws until the end of the items, so
-      // that this launch consumes exactly items + CTAs tickets
+      // that every CTA ends with a ticket past the last item
       if (PERS && !drawn_last)
         while (draw() >= 0) {
         }
+      // The last CTA done drawing returns the slot to zero (the fences order
+      // every CTA's last draw before its done count, and the count before
+      // the reset).
+      if (PERS && n_items > G && a.sched != nullptr) {
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1ull) == static_cast<unsigned long long>(G - 1)) {
+          __threadfence();
+          atomicExch(a.sched, 0ull);
+          atomicExch(a.sched + 1, 0ull);
+        }
+      }
     }
     __syncwarp();
     __syncthreads();  // teardown rendezvous
@@ -910,7 +924,7 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   AttnArgs b = a;
   b.splits = splits;
   if (items <= sms) return launch_form<T, D, NQ, BN, NS, EMU, false>(tq, tk, tv, b, static_cast<int>(items), st);
-  e = counter_slot(items, &b.sched, &b.sched_base);
+  e = counter_slot(&b.sched);
   if (e != cudaSuccess) return e;
   return launch_form<T, D, NQ, BN, NS, EMU, true>(tq, tk, tv, b, sms, st);
 }

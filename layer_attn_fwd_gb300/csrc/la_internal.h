@@ -45,8 +45,7 @@ struct AttnArgs {
   int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
   int tiles_per_split;        // key tiles handled by one split
   int splits;                 // key-range splits (set by the launcher)
-  unsigned long long* sched;  // work-item ticket counter (set by the launcher)
-  unsigned long long sched_base;  // its value when this launch starts
+  unsigned long long* sched;  // work-item ticket counter and done count (set by the launcher)
   uint32_t* err;              // device error word
   int skip_loads;             // test hook: issue no TMA load, so every wait runs out
 };
@@ -66,10 +65,11 @@ bool attn_shape(la_dtype dt, int D, AttnShape* s);
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const AttnArgs& a, int splits, cudaStream_t st);
 
-// A slot of the device's monotonic counters (attention work tickets) for a
-// launch that will add `tickets` to it; *base is the slot's value when the
-// launch starts.
-cudaError_t counter_slot(long long tickets, unsigned long long** ctr, unsigned long long* base);
+// A slot of the device's attention work-ticket counters: ctr[0] the tickets
+// drawn, ctr[1] the CTAs done drawing.  Both are zero when a launch starts
+// and when it ends, so a launch captured in a CUDA graph can be replayed; a
+// graph must not be replayed on two streams at the same time.
+cudaError_t counter_slot(unsigned long long** ctr);
 
 // Merge split partials into o.
 struct CombineArgs {

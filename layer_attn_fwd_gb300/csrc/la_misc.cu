@@ -17,10 +17,11 @@
 #include "la_device.cuh"
 #include "la_internal.h"
 
-// Monotonic device counters (the attention's work tickets).  Launches take
-// the slots in turn, so that a launch that may overlap the previous one
-// (programmatic dependent launch) never shares one.
-__device__ unsigned long long la_counters[64];
+// The attention's work-ticket counters: per slot a ticket count and a count
+// of CTAs done drawing, both zero between launches (the last CTA of a launch
+// to finish drawing resets them).  Launches take the slots in turn, so that
+// launches that may run at the same time (on other streams) rarely share one.
+__device__ unsigned long long la_counters[2 * 64];
 
 namespace la {
 namespace {
@@ -160,11 +161,10 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t counter_slot(long long tickets, unsigned long long** ctr, unsigned long long* base) {
+cudaError_t counter_slot(unsigned long long** ctr) {
   constexpr int kDev = 64, kSlots = 64;
   static std::mutex mu;
   static unsigned long long* addr[kDev] = {};
-  static unsigned long long next_base[kDev][kSlots] = {};
   static int next_slot[kDev] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -179,9 +179,7 @@ cudaError_t counter_slot(long long tickets, unsigned long long** ctr, unsigned l
   }
   const int slot = next_slot[dev];
   next_slot[dev] = (slot + 1) % kSlots;
-  *ctr = addr[dev] + slot;
-  *base = next_base[dev][slot];
-  next_base[dev][slot] += static_cast<unsigned long long>(tickets);
+  *ctr = addr[dev] + 2 * slot;
   return cudaSuccess;
 }
 
