@@ -10,8 +10,8 @@ causal attention B=8 H=8 S=2048 D=64 (with and without key padding), bf16
 causal attention B=4 H=16 S=4096 D=128, the chunked 100k-token mode (bf16
 causal B=2 H=16 S=100000 D=64, windows of 4096 against a growing cache), the
 small fp32 case B=1 H=2 S=128 D=64 (also per-call latency, direct against
-CUDA-graph replay), and the sublayer with its output projection (fp32 and
-bf16, B=8 S=512 d_model=512).
+CUDA-graph replay), and the sublayer with and without its output
+projection (fp32, bf16 and fp16, B=8 S=512 d_model=512).
 
 FLOPs are algorithmic (useful work only): 2*rows*d*3d for the projection,
 2*rows*d*d for the output projection and 4*D per (query, visible key) pair
@@ -344,8 +344,8 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
     attn_case("fp32-small", "fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False)
 
     def layer_out_case(key, name, dt):
-        """The sublayer with its output projection (la_layer_attn_out), and the
-        output projection alone on the same shapes."""
+        """The sublayer (la_layer_attn), the sublayer with its output projection
+        (la_layer_attn_out), and the output projection alone on the same shapes."""
         if not wanted(key):
             return
         B, S, dm, H = 8, 512, 512, 8
@@ -354,10 +354,12 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
         y = torch.empty_like(x)
         n = api.workspace_size(api.LA_OP_LAYER_ATTN_OUT, B, H, S, S, dm // H, dt)
         ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        ms_l = _time_steps(lambda: api.layer_attn(x, Wq, bq, H, out=y, workspace=ws, stream=stream),
+                           Kx, 3, flush, stream, barrier) / Kx
         ms = _time_steps(lambda: api.layer_attn_out(x, Wq, bq, Wo, bo, H, out=y, workspace=ws, stream=stream),
                          Kx, 3, flush, stream, barrier) / Kx
-        fl = (flops.proj_flops(B, S, dm) + flops.attn_flops(B, H, S, S, dm // H, False)
-              + flops.out_proj_flops(B, S, dm))
+        fl_l = flops.proj_flops(B, S, dm) + flops.attn_flops(B, H, S, S, dm // H, False)
+        fl = fl_l + flops.out_proj_flops(B, S, dm)
         o = api.layer_attn(x, Wq, bq, H, stream=stream)
         wo_ws = torch.empty(max(api.workspace_size(api.LA_OP_OUT_PROJ, 1, H, B * S, B * S, dm // H, dt), 16),
                             dtype=torch.uint8, device=dev)
@@ -366,8 +368,11 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
         fl_o = flops.out_proj_flops(B, S, dm)
         pk = _tensor_peak(dt, peaks)
         tf, tf_o = fl / (ms * 1e-3) / 1e12, fl_o / (ms_o * 1e-3) / 1e12
+        tf_l = fl_l / (ms_l * 1e-3) / 1e12
         res[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / pk, 4),
                      "gflop": round(fl / 1e9, 3),
+                     "sublayer_without_out_proj": {"ms": round(ms_l, 4), "tflops": round(tf_l, 2),
+                                                   "frac_of_tensor_peak": round(tf_l / pk, 4)},
                      "out_proj": {"ms": round(ms_o, 4), "tflops": round(tf_o, 2),
                                   "frac_of_tensor_peak": round(tf_o / pk, 4),
                                   "note": "fp32 includes the Wo^T pre-pass" if dt == torch.float32 else ""}}
@@ -415,6 +420,7 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
     small_latency("small-graph", "fp32 B1 H2 S128 D64 non-causal, per-call latency: direct vs CUDA-graph replay")
     layer_out_case("layer-out-fp32", "sublayer + output projection fp32 B8 S512 d512 H8 non-causal", torch.float32)
     layer_out_case("layer-out-bf16", "sublayer + output projection bf16 B8 S512 d512 H8 non-causal", torch.bfloat16)
+    layer_out_case("layer-out-f16", "sublayer + output projection fp16 B8 S512 d512 H8 non-causal", torch.float16)
     if not wanted("chunked-100k"):
         return res
 
@@ -519,7 +525,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--only", choices=["fp32-causal-2048", "fp32-causal-2048-padded", "bf16-causal-4096",
-                                       "fp32-small", "small-graph", "layer-out-fp32", "layer-out-bf16",
+                                       "fp32-small", "small-graph", "layer-out-fp32", "layer-out-bf16", "layer-out-f16",
                                        "chunked-100k"],
                     help="time one named attention workload alone and print its figures (no contract line)")
     args = ap.parse_args()

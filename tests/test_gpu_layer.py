@@ -55,7 +55,7 @@ def test_layer_fp32_b8_s512_d512():
     assert_close(o, oracle.layer_attn(x, W, b, 8), torch.float32, "layer")
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=_id)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=_id)
 @pytest.mark.parametrize("causal", [False, True])
 def test_layer_small(dtype, causal):
     B, S, dm, H = 3, 150, 256, 2
@@ -152,6 +152,14 @@ def test_layer_out_equals_separate_calls(dtype):
     assert api.get_last_error() == api.LA_OK
     assert torch.equal(y1, api.out_proj(o, Wo1, bo1))
     assert torch.equal(y2, api.out_proj(o, Wo2, bo2))
+
+
+def test_layer_f16_b8_s512_d512():
+    """The sublayer workload in fp16 end to end (x, weights, q/k/v, output)."""
+    x, W, b = inputs.layer_inputs(8, 512, 512, torch.float16, seed=83)
+    o = api.layer_attn(x.cuda(), W.cuda(), b.cuda(), 8)
+    assert api.get_last_error() == api.LA_OK
+    assert_close(o, oracle.layer_attn(x, W, b, 8), torch.float16, "layer f16")
 
 
 def test_layer_bf16_b8_s512_d512_wide_projection_tile():
