@@ -55,6 +55,14 @@ def out_proj_inputs(d_model, dtype=torch.float32, seed=0, bias="zero"):
     return Wo.to(dtype), bo.to(dtype)
 
 
+def ln_inputs(d_model, dtype=torch.float32, seed=0):
+    """LayerNorm gain gamma [d] ~ 1 + N(0, 0.1^2) and shift beta [d] ~ N(0, 0.1^2)."""
+    g = _gen(seed)
+    gamma = 1.0 + 0.1 * torch.randn(d_model, generator=g, dtype=torch.float32)
+    beta = 0.1 * torch.randn(d_model, generator=g, dtype=torch.float32)
+    return gamma.to(dtype), beta.to(dtype)
+
+
 def padding_kv_len(B, S_kv):
     """Key-padding pattern: the first half of the batch keeps 75% of its keys
     (the last quarter is padding); the second half keeps all of them."""

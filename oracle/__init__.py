@@ -59,6 +59,8 @@ def _load():
             lib.oracle_layer_attn.argtypes = [P, P, P, I, P, I, LL, I, I, I, P]
             lib.oracle_out_proj.argtypes = [P, I, P, P, I, P, LL, I, I]
             lib.oracle_layer_attn_out.argtypes = [P, P, P, P, P, I, P, I, LL, I, I, I, P]
+            lib.oracle_layernorm.argtypes = [P, I, P, P, I, P, LL, I, D]
+            lib.oracle_layer_attn_ln.argtypes = [P, P, P, D, P, P, P, P, I, P, I, LL, I, I, I, P]
             lib.oracle_widen.argtypes = [P, I, LL]
             lib.oracle_widen.restype = D
             lib.oracle_num_threads.restype = I
@@ -268,6 +270,37 @@ def layer_attn_out(x, W, bias, Wo, bo, H, causal=False, kv_len=None):
     y = np.zeros((B, S, dm))
     _check(_load().oracle_layer_attn_out(_ptr(xb), _ptr(wb), _ptr(bb), _ptr(wob), _ptr(bob), dt, _ptr(y),
                                          B, S, dm, H, int(bool(causal)), _ptr(kl)), "layer_attn_out")
+    return y
+
+
+def layernorm(x, gamma, beta, eps=1e-5):
+    """LayerNorm over the last dimension of x (any supported type; gamma and
+    beta [d] share one type): fp64, biased variance."""
+    xb, dtx = _as_buffer(x)
+    (gb, bb), dtg = _same_type(gamma, beta)
+    d = xb.shape[-1]
+    if gb.shape != (d,) or bb.shape != (d,):
+        raise ValueError("oracle: gamma and beta must have shape [d]")
+    M = xb.size // d
+    y = np.zeros(xb.shape, dtype=np.float64)
+    _check(_load().oracle_layernorm(_ptr(xb), dtx, _ptr(gb), _ptr(bb), dtg, _ptr(y), M, d, float(eps)),
+           "layernorm")
+    return y
+
+
+def layer_attn_ln(x, gamma, beta, W, bias, Wo, bo, H, causal=False, kv_len=None, eps=1e-5):
+    """The pre-norm block: LayerNorm, the sublayer, then (Wo given) the
+    output projection: [B,S,d]."""
+    ts = [x, gamma, beta, W] + [t for t in (bias, Wo, bo) if t is not None]
+    _, dt = _same_type(*ts)
+    xb, gb, btb, wb = (_as_buffer(t)[0] for t in (x, gamma, beta, W))
+    bb, wob, bob = (None if t is None else _as_buffer(t)[0] for t in (bias, Wo, bo))
+    B, S, dm = xb.shape
+    kl = _kvlen(kv_len, B)
+    y = np.zeros((B, S, dm))
+    _check(_load().oracle_layer_attn_ln(_ptr(xb), _ptr(gb), _ptr(btb), float(eps), _ptr(wb), _ptr(bb), _ptr(wob),
+                                        _ptr(bob), dt, _ptr(y), B, S, dm, H, int(bool(causal)), _ptr(kl)),
+           "layer_attn_ln")
     return y
 
 

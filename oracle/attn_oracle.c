@@ -30,13 +30,18 @@
  *   - Output projection y = o Wo + bo after the heads are merged: the
  *     fourth d x d projection of the layer ("Shape-Aware Attention", section
  *     How we built it: the 8BSd^2 term counts Q, K, V and output).
+ *   - LayerNorm before the projection (the pre-norm block): "Shape-Aware
+ *     Attention", section What's next (fusing LayerNorm).
  *
  * Readings taken where the pages are silent:
  *   - a query row with no valid key returns a zero row;
  *   - inputs are the exact stored values (fp32, bf16 or fp16) widened to fp64;
  *     nothing is rounded inside the oracle.
  *   - the sublayer's attention output enters the output projection
- *     unrounded (the GPU stores it in the model's element type first).
+ *     unrounded (the GPU stores it in the model's element type first);
+ *     likewise the normalised activations enter the projection unrounded;
+ *   - LayerNorm divides by sqrt(var + eps) with the biased variance (the
+ *     mean of squared deviations), eps a parameter.
  *
  * Every function here is pinned by tests that do not re-type its formula:
  * closed forms (Q = 0 gives the mean of V, S_kv = 1 returns v_0, two keys give
@@ -456,10 +461,12 @@ int oracle_attn_chunked(const void *q, const void *k, const void *v, int dt, dou
  * Wqkv [d_model, 3 d_model] (columns: the Q block, then K, then V; head h owns
  * columns h*D .. h*D+D-1 of each block), bqkv [3 d_model] or NULL.
  * Outputs q, k, v are head-major [B,H,S,D] fp64; q is multiplied by q_scale.
+ * x has element type dt_x, Wqkv and bqkv dt_w (the pre-norm block passes its
+ * fp64 normalised activations).
  */
-int oracle_qkv_proj(const void *x, const void *W, const void *bias, int dt,
-                    double *q, double *k, double *v,
-                    int B, long long S, int d_model, int H, double q_scale)
+static int qkv_proj_mixed(const void *x, int dt_x, const void *W, const void *bias, int dt_w,
+                          double *q, double *k, double *v,
+                          int B, long long S, int d_model, int H, double q_scale)
 {
     if (H <= 0 || d_model % H) return -1;
     int D = d_model / H;
@@ -472,8 +479,8 @@ int oracle_qkv_proj(const void *x, const void *W, const void *bias, int dt,
         for (long long n = 0; n < N; ++n) {
             double y = 0.0;
             for (int c = 0; c < d_model; ++c)
-                y += load(x, dt, r * d_model + c) * load(W, dt, (long long)c * N + n);
-            if (bias) y += load(bias, dt, n);
+                y += load(x, dt_x, r * d_model + c) * load(W, dt_w, (long long)c * N + n);
+            if (bias) y += load(bias, dt_w, n);
             int which = (int)(n / d_model);
             int h = (int)((n % d_model) / D);
             int d = (int)(n % D);
@@ -486,15 +493,22 @@ int oracle_qkv_proj(const void *x, const void *W, const void *bias, int dt,
     return 0;
 }
 
+int oracle_qkv_proj(const void *x, const void *W, const void *bias, int dt,
+                    double *q, double *k, double *v,
+                    int B, long long S, int d_model, int H, double q_scale)
+{
+    return qkv_proj_mixed(x, dt, W, bias, dt, q, k, v, B, S, d_model, H, q_scale);
+}
+
 /*
  * The attention sublayer as the layer runs it: the fused projection, then
  * attention per head with scale 1/sqrt(D), heads merged back into
  * o [B, S, d_model] (head h in columns h*D .. h*D+D-1).  The output
- * projection is not part of it.
+ * projection is not part of it.  x has element type dt_x, the weights dt_w.
  */
-int oracle_layer_attn(const void *x, const void *W, const void *bias, int dt, double *o,
-                      int B, long long S, int d_model, int H, int causal,
-                      const int32_t *kv_len)
+static int layer_attn_mixed(const void *x, int dt_x, const void *W, const void *bias, int dt_w, double *o,
+                            int B, long long S, int d_model, int H, int causal,
+                            const int32_t *kv_len)
 {
     if (H <= 0 || d_model % H) return -1;
     int D = d_model / H;
@@ -505,7 +519,7 @@ int oracle_layer_attn(const void *x, const void *W, const void *bias, int dt, do
     double *oh = (double *)malloc(sizeof(double) * (n ? n : 1));
     int rc = -1;
     if (q && k && v && oh) {
-        rc = oracle_qkv_proj(x, W, bias, dt, q, k, v, B, S, d_model, H, 1.0);
+        rc = qkv_proj_mixed(x, dt_x, W, bias, dt_w, q, k, v, B, S, d_model, H, 1.0);
         if (rc == 0)
             rc = oracle_attn(q, k, v, ORC_F64, oh, B, H, S, S, D, causal, 1.0 / sqrt((double)D), kv_len);
         if (rc == 0)
@@ -521,6 +535,13 @@ int oracle_layer_attn(const void *x, const void *W, const void *bias, int dt, do
     free(v);
     free(oh);
     return rc;
+}
+
+int oracle_layer_attn(const void *x, const void *W, const void *bias, int dt, double *o,
+                      int B, long long S, int d_model, int H, int causal,
+                      const int32_t *kv_len)
+{
+    return layer_attn_mixed(x, dt, W, bias, dt, o, B, S, d_model, H, causal, kv_len);
 }
 
 /*
@@ -551,19 +572,82 @@ int oracle_out_proj(const void *a, int dt_a, const void *W, const void *bias, in
 /*
  * The sublayer with its output projection: oracle_layer_attn, then
  * oracle_out_proj (d_model -> d_model) applied to its fp64 result, which is
- * not rounded in between.  y [B, S, d_model].
+ * not rounded in between.  y [B, S, d_model].  x has element type dt_x, the
+ * weights dt_w.
  */
+static int layer_attn_out_mixed(const void *x, int dt_x, const void *Wqkv, const void *bqkv,
+                                const void *Wo, const void *bo, int dt_w, double *y,
+                                int B, long long S, int d_model, int H, int causal,
+                                const int32_t *kv_len)
+{
+    size_t n = (size_t)B * S * d_model;
+    double *o = (double *)malloc(sizeof(double) * (n ? n : 1));
+    if (!o) return -1;
+    int rc = layer_attn_mixed(x, dt_x, Wqkv, bqkv, dt_w, o, B, S, d_model, H, causal, kv_len);
+    if (rc == 0) rc = oracle_out_proj(o, ORC_F64, Wo, bo, dt_w, y, (long long)B * S, d_model, d_model);
+    free(o);
+    return rc;
+}
+
 int oracle_layer_attn_out(const void *x, const void *Wqkv, const void *bqkv,
                           const void *Wo, const void *bo, int dt, double *y,
                           int B, long long S, int d_model, int H, int causal,
                           const int32_t *kv_len)
 {
+    return layer_attn_out_mixed(x, dt, Wqkv, bqkv, Wo, bo, dt, y, B, S, d_model, H, causal, kv_len);
+}
+
+/*
+ * LayerNorm over the last dimension ("Shape-Aware Attention", section
+ * What's next: fusing LayerNorm; "GPU Kernel for a Transformer Layer",
+ * section What we learned: its statistics are reductions kept in full
+ * precision):
+ *   mu_r = mean_c x[r,c],  var_r = mean_c (x[r,c] - mu_r)^2   (biased)
+ *   y[r,c] = (x[r,c] - mu_r) / sqrt(var_r + eps) * gamma[c] + beta[c]
+ * x [M, d] in element type dt_x (fp64 allowed), gamma and beta [d] in dt_g.
+ */
+int oracle_layernorm(const void *x, int dt_x, const void *gamma, const void *beta, int dt_g,
+                     double *y, long long M, int d, double eps)
+{
+    if (M < 0 || d < 1 || !(eps >= 0.0)) return -1;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long long r = 0; r < M; ++r) {
+        double mu = 0.0, var = 0.0;
+        for (int c = 0; c < d; ++c) mu += load(x, dt_x, r * d + c);
+        mu /= d;
+        for (int c = 0; c < d; ++c) {
+            double t = load(x, dt_x, r * d + c) - mu;
+            var += t * t;
+        }
+        var /= d;
+        double rstd = 1.0 / sqrt(var + eps);
+        for (int c = 0; c < d; ++c)
+            y[r * d + c] = (load(x, dt_x, r * d + c) - mu) * rstd * load(gamma, dt_g, c) + load(beta, dt_g, c);
+    }
+    return 0;
+}
+
+/*
+ * The pre-norm attention block: LayerNorm, then the sublayer (projection,
+ * attention, heads merged), then the output projection when Wo is given.
+ * Intermediate results stay in fp64.  y [B, S, d_model].
+ */
+int oracle_layer_attn_ln(const void *x, const void *gamma, const void *beta, double eps,
+                         const void *Wqkv, const void *bqkv, const void *Wo, const void *bo, int dt,
+                         double *y, int B, long long S, int d_model, int H, int causal,
+                         const int32_t *kv_len)
+{
     size_t n = (size_t)B * S * d_model;
-    double *o = (double *)malloc(sizeof(double) * (n ? n : 1));
-    if (!o) return -1;
-    int rc = oracle_layer_attn(x, Wqkv, bqkv, dt, o, B, S, d_model, H, causal, kv_len);
-    if (rc == 0) rc = oracle_out_proj(o, ORC_F64, Wo, bo, dt, y, (long long)B * S, d_model, d_model);
-    free(o);
+    double *xn = (double *)malloc(sizeof(double) * (n ? n : 1));
+    if (!xn) return -1;
+    int rc = oracle_layernorm(x, dt, gamma, beta, dt, xn, (long long)B * S, d_model, eps);
+    if (rc == 0) {
+        if (Wo)
+            rc = layer_attn_out_mixed(xn, ORC_F64, Wqkv, bqkv, Wo, bo, dt, y, B, S, d_model, H, causal, kv_len);
+        else
+            rc = layer_attn_mixed(xn, ORC_F64, Wqkv, bqkv, dt, y, B, S, d_model, H, causal, kv_len);
+    }
+    free(xn);
     return rc;
 }
 

@@ -399,3 +399,71 @@ def test_layer_attn_out_identity_weight_is_layer_attn():
     eye = torch.eye(dm, dtype=torch.float32)
     y = oracle.layer_attn_out(x, W, b, eye, None, H, causal=True)
     assert np.array_equal(y, oracle.layer_attn(x, W, b, H, causal=True))
+
+
+# --------------------------------------------------------------------------
+# LayerNorm and the pre-norm block
+# --------------------------------------------------------------------------
+def test_layernorm_closed_form_row():
+    """x = [1, 2, 3, 4]: mean 2.5, biased variance 1.25, so with eps = 0 the
+    normalised row is [-3, -1, 1, 3] / sqrt(5); then gamma and beta per column."""
+    x = torch.tensor([[1.0, 2.0, 3.0, 4.0]], dtype=torch.float64)
+    g = torch.tensor([1.0, 2.0, 3.0, 4.0], dtype=torch.float64)
+    b = torch.tensor([10.0, 20.0, 30.0, 40.0], dtype=torch.float64)
+    y = oracle.layernorm(x, g, b, eps=0.0)
+    want = np.array([-3.0, -1.0, 1.0, 3.0]) / math.sqrt(5.0) * g.numpy() + b.numpy()
+    assert np.allclose(y[0], want, atol=1e-14, rtol=0)
+
+
+def test_layernorm_moments_with_eps():
+    """gamma = 1, beta = 0: every row has mean 0 and mean square var/(var+eps)."""
+    g = torch.Generator().manual_seed(67)
+    x = 3.0 + 2.0 * torch.randn(6, 96, generator=g, dtype=torch.float64)
+    eps = 0.1
+    y = oracle.layernorm(x, torch.ones(96, dtype=torch.float64), torch.zeros(96, dtype=torch.float64), eps=eps)
+    var = x.var(dim=1, unbiased=False).numpy()
+    assert np.allclose(y.mean(axis=1), 0.0, atol=1e-13)
+    assert np.allclose((y * y).mean(axis=1), var / (var + eps), atol=1e-13, rtol=0)
+
+
+def test_layernorm_affine_invariance():
+    """With eps = 0, LN(a x + c) = sign(a) LN(x) for a row-wise shift c."""
+    g = torch.Generator().manual_seed(68)
+    x = torch.randn(5, 64, generator=g, dtype=torch.float64)
+    gam = torch.randn(64, generator=g, dtype=torch.float64)
+    bet = torch.randn(64, generator=g, dtype=torch.float64)
+    base = oracle.layernorm(x, gam, bet, eps=0.0)
+    c = torch.randn(5, 1, generator=g, dtype=torch.float64) * 10
+    assert np.allclose(oracle.layernorm(7.5 * x + c, gam, bet, eps=0.0), base, atol=1e-12)
+    flipped = oracle.layernorm(-2.0 * x + c, gam, bet, eps=0.0)
+    assert np.allclose(flipped - bet.numpy(), -(base - bet.numpy()), atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_layernorm_matches_torch_float64(dtype):
+    g = torch.Generator().manual_seed(69)
+    x = (1.5 + torch.randn(2, 7, 128, generator=g)).to(dtype)
+    gam = (1.0 + 0.1 * torch.randn(128, generator=g)).to(dtype)
+    bet = (0.1 * torch.randn(128, generator=g)).to(dtype)
+    want = F.layer_norm(x.double(), (128,), gam.double(), bet.double(), eps=1e-5).numpy()
+    assert np.allclose(oracle.layernorm(x, gam, bet, eps=1e-5), want, atol=1e-12, rtol=1e-12)
+
+
+@pytest.mark.parametrize("with_out", [False, True])
+def test_layer_attn_ln_matches_library_pipeline(with_out):
+    """torch float64 layer_norm, then the oracle's sublayer pipeline in
+    torch (projection, SDPA, merge) and the output projection."""
+    B, S, dm, H = 2, 9, 32, 4
+    x, W, b = inputs.layer_inputs(B, S, dm, seed=70, bias="normal")
+    gam, bet = inputs.ln_inputs(dm, seed=71)
+    Wo, bo = inputs.out_proj_inputs(dm, seed=72, bias="normal") if with_out else (None, None)
+    kv_len = torch.tensor([9, 4], dtype=torch.int32)
+    y = oracle.layer_attn_ln(x, gam, bet, W, b, Wo, bo, H, causal=True, kv_len=kv_len, eps=1e-5)
+    xn = F.layer_norm(x.double(), (dm,), gam.double(), bet.double(), eps=1e-5).numpy()
+    D = dm // H
+    p = torch.from_numpy(xn.reshape(B * S, dm) @ _np(W) + _np(b)).reshape(B, S, 3, H, D)
+    q, k, v = (p[:, :, t].transpose(1, 2).contiguous() for t in range(3))
+    o, _ = _sdpa64(q, k, v, True, kv_len)
+    o = o.transpose(0, 2, 1, 3).reshape(B * S, dm)
+    want = (o @ _np(Wo) + _np(bo)) if with_out else o
+    assert np.allclose(y, want.reshape(B, S, dm), atol=1e-12, rtol=1e-12)
