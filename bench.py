@@ -11,7 +11,8 @@ causal attention B=4 H=16 S=4096 D=128, the chunked 100k-token mode (bf16
 causal B=2 H=16 S=100000 D=64, windows of 4096 against a growing cache), the
 small fp32 case B=1 H=2 S=128 D=64 (also per-call latency, direct against
 CUDA-graph replay), and the sublayer with and without its output
-projection (fp32, bf16 and fp16, B=8 S=512 d_model=512).
+projection and with a LayerNorm in front (fp32, bf16 and fp16, B=8 S=512
+d_model=512).
 
 FLOPs are algorithmic (useful work only): 2*rows*d*3d for the projection,
 2*rows*d*d for the output projection and 4*D per (query, visible key) pair
@@ -345,19 +346,23 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
 
     def layer_out_case(key, name, dt):
         """The sublayer (la_layer_attn), the sublayer with its output projection
-        (la_layer_attn_out), and the output projection alone on the same shapes."""
+        (la_layer_attn_out), the pre-norm block (la_layer_attn_ln: LayerNorm,
+        sublayer, output projection), and the output projection alone."""
         if not wanted(key):
             return
         B, S, dm, H = 8, 512, 512, 8
         x, Wq, bq = (t.to(dev) for t in inputs.layer_inputs(B, S, dm, dt, seed=0))
         Wo, bo = (t.to(dev) for t in inputs.out_proj_inputs(dm, dt, seed=1))
         y = torch.empty_like(x)
-        n = api.workspace_size(api.LA_OP_LAYER_ATTN_OUT, B, H, S, S, dm // H, dt)
+        gam, bet = (t.to(dev) for t in inputs.ln_inputs(dm, dt, seed=2))
+        n = api.workspace_size(api.LA_OP_LAYER_ATTN_LN, B, H, S, S, dm // H, dt)
         ws = torch.empty(n, dtype=torch.uint8, device=dev)
         ms_l = _time_steps(lambda: api.layer_attn(x, Wq, bq, H, out=y, workspace=ws, stream=stream),
                            Kx, 3, flush, stream, barrier) / Kx
         ms = _time_steps(lambda: api.layer_attn_out(x, Wq, bq, Wo, bo, H, out=y, workspace=ws, stream=stream),
                          Kx, 3, flush, stream, barrier) / Kx
+        ms_ln = _time_steps(lambda: api.layer_attn_ln(x, gam, bet, Wq, bq, Wo, bo, H, out=y, workspace=ws,
+                                                      stream=stream), Kx, 3, flush, stream, barrier) / Kx
         fl_l = flops.proj_flops(B, S, dm) + flops.attn_flops(B, H, S, S, dm // H, False)
         fl = fl_l + flops.out_proj_flops(B, S, dm)
         o = api.layer_attn(x, Wq, bq, H, stream=stream)
@@ -373,10 +378,12 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
                      "gflop": round(fl / 1e9, 3),
                      "sublayer_without_out_proj": {"ms": round(ms_l, 4), "tflops": round(tf_l, 2),
                                                    "frac_of_tensor_peak": round(tf_l / pk, 4)},
+                     "prenorm_block": {"ms": round(ms_ln, 4), "layernorm_cost_ms": round(ms_ln - ms, 4),
+                                       "note": "LayerNorm + sublayer + output projection"},
                      "out_proj": {"ms": round(ms_o, 4), "tflops": round(tf_o, 2),
                                   "frac_of_tensor_peak": round(tf_o / pk, 4),
                                   "note": "fp32 includes the Wo^T pre-pass" if dt == torch.float32 else ""}}
-        del x, Wq, bq, Wo, bo, y, ws, o, wo_ws
+        del x, Wq, bq, Wo, bo, y, ws, o, wo_ws, gam, bet
 
     def small_latency(key, name):
         """Small-shape latency: back-to-back calls, host wall clock per call

@@ -74,7 +74,8 @@ typedef enum {
     LA_OP_LAYER_ATTN = 2,
     LA_OP_QKV_PROJ = 3,
     LA_OP_OUT_PROJ = 4,
-    LA_OP_LAYER_ATTN_OUT = 5
+    LA_OP_LAYER_ATTN_OUT = 5,
+    LA_OP_LAYER_ATTN_LN = 6
 } la_op;
 
 /*
@@ -216,6 +217,43 @@ la_status la_layer_attn_out(const void *x, const void *Wqkv, const void *bqkv,
                             void *ws, size_t ws_bytes, la_stream_t st);
 
 /*
+ * LayerNorm over the last dimension, the normalisation in front of the
+ * attention sublayer of a pre-norm layer ("Shape-Aware Attention", section
+ * What's next: fusing LayerNorm; statistics in fp32 as "GPU Kernel for a
+ * Transformer Layer", section What we learned, asks of reductions):
+ *   y[r, c] = (x[r, c] - mean_r) / sqrt(var_r + eps) * gamma[c] + beta[c]
+ * with mean_r and the biased variance var_r (mean squared deviation) of row
+ * r, computed in fp32 in two passes over the row.
+ *   x, y  [M, d] row-major (may be the same buffer); gamma, beta [d]
+ * d must be a positive multiple of 64 (else LA_ERR_UNSUPPORTED); eps >= 0
+ * and finite; all four pointers 16-byte aligned.  M == 0 is a no-op.
+ * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED or LA_ERR_CUDA.
+ */
+la_status la_layernorm(const void *x, const void *gamma, const void *beta, void *y,
+                       int M, int d, float eps, la_dtype dt, la_stream_t st);
+
+/*
+ * The pre-norm attention block: la_layernorm(x), then the sublayer of
+ * la_layer_attn on the normalised activations (stored in the element type
+ * dt in between), then, when Wo is not NULL, the output projection of
+ * la_out_proj:
+ *   y [B, S, d_model] = [merge_heads(attention(LN(x) . Wqkv + bqkv)) . Wo + bo]
+ * gamma, beta [d_model] and eps as for la_layernorm; Wo [d_model, d_model]
+ * and bo [d_model] may be NULL (bo must be NULL when Wo is).  Arguments
+ * otherwise as for la_layer_attn.  The layer's residual add is not part of
+ * it.  ws must hold at least
+ * la_workspace_size(LA_OP_LAYER_ATTN_LN, B, H, S, S, d_model / H, dt) bytes
+ * (sized for the output projection; without it less is needed); otherwise
+ * LA_ERR_WORKSPACE.
+ */
+la_status la_layer_attn_ln(const void *x, const void *gamma, const void *beta, float eps,
+                           const void *Wqkv, const void *bqkv,
+                           const void *Wo, const void *bo, void *y,
+                           int B, int S, int d_model, int H, int causal,
+                           const int32_t *kv_len, la_dtype dt,
+                           void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
  * la_attn_fwd without a workspace, for callers that cannot allocate device
  * memory: a host framework whose plugin interface hands over only the input
  * and output tensors, a service that sizes all of its device memory once at
@@ -250,7 +288,8 @@ la_status la_attn_fwd_noalloc(const void *q, const void *k, const void *v, void 
  * Workspace bytes an operation wants (0 if none).  op is an la_op; the
  * remaining arguments are those of the call (for LA_OP_ATTN_CHUNKED pass
  * S_q = chunk and S_kv = the cache's S_max; for LA_OP_LAYER_ATTN,
- * LA_OP_LAYER_ATTN_OUT and LA_OP_QKV_PROJ pass S_q = S_kv = S and
+ * LA_OP_LAYER_ATTN_OUT, LA_OP_LAYER_ATTN_LN and LA_OP_QKV_PROJ pass S_q =
+ * S_kv = S and
  * D = d_model / H; for LA_OP_OUT_PROJ see la_out_proj).  Returns (size_t)-1
  * for invalid arguments.  Host only; touches no device.
  */

@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "liblayerattn.so")
 
 LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_INTERNAL = range(7)
 LA_F32, LA_BF16, LA_F16 = 0, 1, 2
-LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN, LA_OP_QKV_PROJ, LA_OP_OUT_PROJ, LA_OP_LAYER_ATTN_OUT = range(6)
+(LA_OP_ATTN_FWD, LA_OP_ATTN_CHUNKED, LA_OP_LAYER_ATTN, LA_OP_QKV_PROJ, LA_OP_OUT_PROJ, LA_OP_LAYER_ATTN_OUT,
+ LA_OP_LAYER_ATTN_LN) = range(7)
 
 _DT = {torch.float32: LA_F32, torch.bfloat16: LA_BF16, torch.float16: LA_F16}
 
@@ -59,6 +60,8 @@ def load(path: str | None = None):
         lib.la_layer_attn.argtypes = [P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
         lib.la_out_proj.argtypes = [P, P, P, P, I, I, I, P, Z, P]
         lib.la_layer_attn_out.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
+        lib.la_layernorm.argtypes = [P, P, P, P, I, I, F, I, P]
+        lib.la_layer_attn_ln.argtypes = [P, P, P, F, P, P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
         lib.la_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.la_workspace_size.restype = Z
         lib.la_get_last_error.argtypes = [P]
@@ -69,7 +72,7 @@ def load(path: str | None = None):
         lib.la_status_string.argtypes = [I]
         lib.la_status_string.restype = ctypes.c_char_p
         for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_out_proj",
-                     "la_layer_attn_out", "la_get_last_error"):
+                     "la_layer_attn_out", "la_layernorm", "la_layer_attn_ln", "la_get_last_error"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -265,6 +268,35 @@ def layer_attn_out(x, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=None, out=None
     _check(load().la_layer_attn_out(_ptr(x), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), _ptr(y), B, S, dm, H,
                                     int(bool(causal)), _ptr(kv_len), _dt(x), _ptr(workspace), nbytes,
                                     _stream(stream)), "la_layer_attn_out")
+    return y
+
+
+def layernorm(x, gamma, beta, eps=1e-5, out=None, stream=None):
+    """LayerNorm over the last dimension of x (rows of d, d a multiple of 64)."""
+    for t, n in ((x, "x"), (gamma, "gamma"), (beta, "beta")):
+        _need(t, n)
+    d = x.shape[-1]
+    M = x.numel() // d if d > 0 else 0
+    y = torch.empty_like(x) if out is None else out
+    _check(load().la_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), M, d, float(eps), _dt(x),
+                               _stream(stream)), "la_layernorm")
+    return y
+
+
+def layer_attn_ln(x, gamma, beta, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=None, eps=1e-5, out=None,
+                  workspace=None, stream=None):
+    """The pre-norm attention block: LayerNorm, the sublayer and (Wo not None)
+    the output projection: x [B,S,d] -> [B,S,d]."""
+    _need(x, "x")
+    B, S, dm = x.shape
+    D = dm // H if H > 0 else 0
+    y = torch.empty_like(x) if out is None else out
+    if workspace is None:
+        workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN_LN, B, H, S, S, D, x.dtype), x.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_layer_attn_ln(_ptr(x), _ptr(gamma), _ptr(beta), float(eps), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo),
+                                   _ptr(bo), _ptr(y), B, S, dm, H, int(bool(causal)), _ptr(kv_len), _dt(x),
+                                   _ptr(workspace), nbytes, _stream(stream)), "la_layer_attn_ln")
     return y
 
 

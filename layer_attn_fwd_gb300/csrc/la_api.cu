@@ -460,6 +460,59 @@ la_status check_layer_args(const void* x, const void* Wqkv, const void* bqkv, co
   return LA_OK;
 }
 
+la_status check_ln_args(const void* gamma, const void* beta, float eps) {
+  if (!gamma || !beta) return LA_ERR_INVALID;
+  if (!aligned16(gamma) || !aligned16(beta)) return LA_ERR_INVALID;
+  if (!(eps >= 0.f) || !isfinite(eps)) return LA_ERR_INVALID;
+  return LA_OK;
+}
+
+// Workspace of the block: the normalised x (with LayerNorm) | the merged
+// attention output and the fp32 Wo^T (with the output projection) | the
+// sublayer's own workspace.
+size_t block_fixed_bytes(int B, int S, int d_model, int H, la_dtype dt, bool ln, bool out) {
+  const size_t act = layer_qkv_bytes(B, S, d_model, dt);
+  return (ln ? act : 0) + (out ? act + wot_bytes(dt, d_model) : 0) + layer_fixed_bytes(B, S, d_model, H, dt);
+}
+
+// The attention block: [LayerNorm] -> projection -> attention (heads merged)
+// -> [output projection].  Arguments already validated.  For fp32 the
+// weight transposes come first: Wqkv^T as an ordinary launch (everything
+// before this call has finished), then Wo^T and the LayerNorm, which may
+// overlap it (each waits for the grid before it before exiting).
+la_status run_block(const void* x, const void* gamma, const void* beta, float eps, const void* Wqkv,
+                    const void* bqkv, const void* Wo, const void* bo, void* y, int B, int S, int d_model, int H,
+                    int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes, cudaStream_t cs) {
+  const bool ln = gamma != nullptr, out = Wo != nullptr;
+  if (ws_bytes < block_fixed_bytes(B, S, d_model, H, dt, ln, out)) return LA_ERR_WORKSPACE;
+  if (S == 0) return LA_OK;
+  const size_t act = layer_qkv_bytes(B, S, d_model, dt);
+  const long long M = static_cast<long long>(B) * S;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* xn = ln ? w : nullptr;
+  w += ln ? act : 0;
+  void* o = out ? w : y;
+  void* wot = out ? w + act : nullptr;
+  w += out ? act + wot_bytes(dt, d_model) : 0;
+  const size_t lw_bytes = ws_bytes - static_cast<size_t>(w - static_cast<uint8_t*>(ws));
+  bool first = true;  // the first launch of the call is an ordinary one
+  if (dt == LA_F32) {
+    uint8_t* wt = w + 2 * act + vt_bytes(dt, B, H, S, d_model / H);  // where run_layer keeps Wqkv^T
+    if (launch_transpose32(Wqkv, 0, wt, d_model, 1, d_model, 3 * d_model, cs) != cudaSuccess) return LA_ERR_CUDA;
+    first = false;
+    if (out && launch_transpose32(Wo, 0, wot, d_model, 1, d_model, d_model, cs, true) != cudaSuccess)
+      return LA_ERR_CUDA;
+  }
+  if (ln) {
+    if (launch_layernorm(dt, x, gamma, beta, xn, M, d_model, eps, cs, !first) != cudaSuccess) return LA_ERR_CUDA;
+    first = false;
+  }
+  la_status s = run_layer(ln ? xn : x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, w, lw_bytes,
+                          dt == LA_F32, cs);
+  if (s != LA_OK || !out) return s;
+  return run_out_proj(o, Wo, wot, bo, y, M, d_model, dt, cs);
+}
+
 }  // namespace
 }  // namespace la
 
@@ -553,28 +606,38 @@ la_status la_layer_attn_out(const void* x, const void* Wqkv, const void* bqkv, c
   if (s != LA_OK) return s;
   s = check_out_proj_args(ws, Wo, bo, y, static_cast<long long>(B) * S, d_model, dt);
   if (s != LA_OK) return s;
-  // ws: heads-merged attention output o [B,S,d] | fp32 Wo^T | the sublayer's own workspace
-  const size_t obytes = layer_qkv_bytes(B, S, d_model, dt);
-  const size_t wob = wot_bytes(dt, d_model);
-  if (ws_bytes < obytes + wob + layer_fixed_bytes(B, S, d_model, H, dt)) return LA_ERR_WORKSPACE;
-  if (S == 0) return LA_OK;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  void* o = w;
-  void* wot = w + obytes;
-  uint8_t* lw = w + obytes + wob;
-  const size_t lw_bytes = ws_bytes - obytes - wob;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
-  if (dt == LA_F32) {
-    // both weight transposes first: Wqkv^T (an ordinary launch, so everything
-    // before this call has finished), then Wo^T, which may overlap it
-    const size_t one = layer_qkv_bytes(B, S, d_model, dt);
-    uint8_t* wt = lw + 2 * one + vt_bytes(dt, B, H, S, d_model / H);
-    if (launch_transpose32(Wqkv, 0, wt, d_model, 1, d_model, 3 * d_model, cs) != cudaSuccess) return LA_ERR_CUDA;
-    if (launch_transpose32(Wo, 0, wot, d_model, 1, d_model, d_model, cs, true) != cudaSuccess) return LA_ERR_CUDA;
-  }
-  s = run_layer(x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, lw, lw_bytes, dt == LA_F32, cs);
+  return run_block(x, nullptr, nullptr, 0.f, Wqkv, bqkv, Wo, bo, y, B, S, d_model, H, causal, kv_len, dt, ws,
+                   ws_bytes, reinterpret_cast<cudaStream_t>(st));
+}
+
+la_status la_layernorm(const void* x, const void* gamma, const void* beta, void* y, int M, int d, float eps,
+                       la_dtype dt, la_stream_t st) {
+  if (!x || !y) return LA_ERR_INVALID;
+  if (M < 0 || d < 1 || !dtype_ok(dt)) return LA_ERR_INVALID;
+  la_status s = check_ln_args(gamma, beta, eps);
   if (s != LA_OK) return s;
-  return run_out_proj(o, Wo, wot, bo, y, static_cast<long long>(B) * S, d_model, dt, cs);
+  if (d % 64 != 0) return LA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y)) return LA_ERR_INVALID;
+  if (M == 0) return LA_OK;
+  return cuda_status(launch_layernorm(dt, x, gamma, beta, y, M, d, eps, reinterpret_cast<cudaStream_t>(st)));
+}
+
+la_status la_layer_attn_ln(const void* x, const void* gamma, const void* beta, float eps, const void* Wqkv,
+                           const void* bqkv, const void* Wo, const void* bo, void* y, int B, int S, int d_model,
+                           int H, int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes,
+                           la_stream_t st) {
+  la_status s = check_layer_args(x, Wqkv, bqkv, y, ws, B, S, d_model, H, kv_len, dt);
+  if (s != LA_OK) return s;
+  s = check_ln_args(gamma, beta, eps);
+  if (s != LA_OK) return s;
+  if (Wo != nullptr) {
+    s = check_out_proj_args(ws, Wo, bo, y, static_cast<long long>(B) * S, d_model, dt);
+    if (s != LA_OK) return s;
+  } else if (bo != nullptr) {
+    return LA_ERR_INVALID;
+  }
+  return run_block(x, gamma, beta, eps, Wqkv, bqkv, Wo, bo, y, B, S, d_model, H, causal, kv_len, dt, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(st));
 }
 
 size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt) {
@@ -592,10 +655,10 @@ size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtyp
       return wt_bytes(dt, H * D);
     case LA_OP_OUT_PROJ:
       return wot_bytes(dt, H * D);
-    case LA_OP_LAYER_ATTN_OUT: {
+    case LA_OP_LAYER_ATTN_OUT:
+    case LA_OP_LAYER_ATTN_LN: {
       if (S_q != S_kv) return bad;
-      const int dm = H * D;
-      return layer_qkv_bytes(B, S_q, dm, dt) + wot_bytes(dt, dm) + layer_fixed_bytes(B, S_q, dm, H, dt) +
+      return block_fixed_bytes(B, S_q, H * D, H, dt, op == LA_OP_LAYER_ATTN_LN, true) +
              attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);
     }
     default:

@@ -90,6 +90,11 @@ cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
                                int R, int C, cudaStream_t st, bool pdl = false);
 
+// LayerNorm of M rows of d elements (d a multiple of 64, 16-byte aligned
+// pointers), statistics in fp32.  pdl: as for launch_transpose32.
+cudaError_t launch_layernorm(la_dtype dt, const void* x, const void* gamma, const void* beta, void* y, long long M,
+                             int d, float eps, cudaStream_t st, bool pdl = false);
+
 // Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`.
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
                              int rows, int D, int S_max, int at, int elem_bytes, cudaStream_t st);

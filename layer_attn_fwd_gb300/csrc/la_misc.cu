@@ -6,8 +6,10 @@
 //   - key/value cache append for the chunked long-context mode ("Roofline",
 //     section How we built it: windows against a growing key/value cache);
 //   - a 32-bit batched transpose: the TF32 tensor cores take K-major operands
-//     only, so fp32 V (and the fp32 projection weight) are presented
-//     transposed.
+//     only, so fp32 V (and the fp32 projection weights) are presented
+//     transposed;
+//   - LayerNorm before the projection (the pre-norm block; "Shape-Aware
+//     Attention", section What's next: fusing LayerNorm), statistics in fp32.
 // All are plain coalesced streams with grids sized to the SM count.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -152,6 +154,177 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
 }
 
+// 16 bytes of T <-> fp32 values.
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void unpack(const uint4& w, float* v) {
+    v[0] = __uint_as_float(w.x), v[1] = __uint_as_float(w.y), v[2] = __uint_as_float(w.z), v[3] = __uint_as_float(w.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+  }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  // a bf16 value is the upper half of the fp32 with the same bits
+  static __device__ __forceinline__ void unpack(const uint4& w, float* v) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[2 * i] = __uint_as_float(u[i] << 16), v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* v) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      memcpy(&u[i], &h, 4);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+};
+template <>
+struct Vec16<__half> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void unpack(const uint4& w, float* v) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h;
+      memcpy(&h, &u[i], 4);
+      const float2 f = __half22float2(h);
+      v[2 * i] = f.x, v[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float* v) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+      memcpy(&u[i], &h, 4);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+};
+
+// Sum over aligned groups of G lanes (G a power of two <= 32).
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// LayerNorm of rows of d elements (d a multiple of 64), one group of LPR
+// lanes per row (a warp takes 32 / LPR rows at once): the mean, then the
+// mean squared deviation from it, both in fp32; then
+// y = (x - mean) / sqrt(var + eps) * gamma + beta, rounded to T.  16-byte
+// accesses; rows 16-byte aligned.  A row of up to LPR * FPL values is loaded
+// once (all of a lane's loads issued together) and kept unpacked in
+// registers; gamma and beta, the same for every row, are read when the
+// output is formed.  Longer rows take three passes (the later two hit L1).
+// Every lane of a warp runs the same number of loop trips (rows past the end
+// skip their loads and stores), so the group sums see whole warps.
+template <typename T, int FPL, int LPR>
+__global__ void __launch_bounds__(256, 3)
+    layernorm_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
+                     T* __restrict__ y, long long M, int d, float eps) {
+  using V = Vec16<T>;
+  constexpr int E = V::N;
+  constexpr int NVL = FPL / E;  // 16-byte vectors a lane holds
+  constexpr int RPW = 32 / LPR;  // rows per warp
+  pdl_trigger();  // the next grid may be scheduled now; it waits for this one to finish
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & (LPR - 1);        // lane within the row's group
+  const int grp = (threadIdx.x & 31) / LPR;        // the warp's row this lane works on
+  const int nv = d / E;
+  const float inv_d = 1.f / static_cast<float>(d);
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  const uint4* b4 = reinterpret_cast<const uint4*>(beta);
+  const long long stride = static_cast<long long>(gridDim.x) * 8 * RPW;
+  for (long long r0 = (blockIdx.x * 8LL + warp) * RPW; r0 < M; r0 += stride) {
+    const long long r = r0 + grp;
+    const bool live = r < M;
+    const long long rr = live ? r : r0;  // a dead group reads the warp's first row and stores nothing
+    const uint4* xr = reinterpret_cast<const uint4*>(x + rr * d);
+    uint4* yr = reinterpret_cast<uint4*>(y + rr * d);
+    if (nv <= LPR * NVL) {
+      uint4 w[NVL];
+#pragma unroll
+      for (int j = 0; j < NVL; ++j)
+        if (lane + LPR * j < nv) w[j] = xr[lane + LPR * j];
+      float v[NVL][E];
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < NVL; ++j) {
+        if (lane + LPR * j < nv) {
+          V::unpack(w[j], v[j]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) s += v[j][e];
+        }
+      }
+      const float mu = group_sum<LPR>(s) * inv_d;
+      float q = 0.f;
+#pragma unroll
+      for (int j = 0; j < NVL; ++j)
+        if (lane + LPR * j < nv)
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            v[j][e] -= mu;
+            q = fmaf(v[j][e], v[j][e], q);
+          }
+      const float rstd = 1.f / sqrtf(group_sum<LPR>(q) * inv_d + eps);
+#pragma unroll
+      for (int j = 0; j < NVL; ++j) {
+        const int i = lane + LPR * j;
+        if (live && i < nv) {
+          float g[E], b[E];
+          V::unpack(g4[i], g);
+          V::unpack(b4[i], b);
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[j][e] = fmaf(v[j][e] * rstd, g[e], b[e]);
+          yr[i] = V::pack(v[j]);
+        }
+      }
+    } else {
+      float v[E];
+      float s = 0.f;
+      for (int i = lane; i < nv; i += LPR) {
+        V::unpack(xr[i], v);
+#pragma unroll
+        for (int e = 0; e < E; ++e) s += v[e];
+      }
+      const float mu = group_sum<LPR>(s) * inv_d;
+      float q = 0.f;
+      for (int i = lane; i < nv; i += LPR) {
+        V::unpack(xr[i], v);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float t = v[e] - mu;
+          q = fmaf(t, t, q);
+        }
+      }
+      const float rstd = 1.f / sqrtf(group_sum<LPR>(q) * inv_d + eps);
+      for (int i = lane; i < nv && live; i += LPR) {
+        float g[E], b[E];
+        V::unpack(xr[i], v);
+        V::unpack(g4[i], g);
+        V::unpack(b4[i], b);
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = fmaf((v[e] - mu) * rstd, g[e], b[e]);
+        yr[i] = V::pack(v);
+      }
+    }
+  }
+  // Under programmatic serialization this grid may run beside the one before
+  // it; waiting for that grid before exiting keeps the stream's order for the
+  // grids after this one.  A no-op for an ordinary launch.
+  pdl_wait();
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
@@ -211,6 +384,42 @@ cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, 
   if (pdl) return launch_pdl(transpose32_kernel, grid, dim3(256), 0, st, s, d, R, C, ld_dst, src_batch, dst_batch, vec);
   transpose32_kernel<<<grid, 256, 0, st>>>(s, d, R, C, ld_dst, src_batch, dst_batch, vec);
   return cudaGetLastError();
+}
+
+// Row values each lane keeps in registers (within 80 registers, so three
+// blocks share an SM): rows of up to 32 x 16 fp32 or 32 x 32 half-precision
+// values take the single-pass form.
+constexpr int kLnFloatsPerLaneF32 = 16, kLnFloatsPerLaneHalf = 32;
+
+template <typename T, int FPL>
+cudaError_t launch_ln(const void* x, const void* gamma, const void* beta, void* y, long long M, int d, float eps,
+                      cudaStream_t st, bool pdl) {
+  // Half a warp per row when the row fits in registers that way: twice the
+  // rows per warp, so a launch of a few thousand rows runs in one wave.
+  const bool half_warp = d / Vec16<T>::N <= 16 * (FPL / Vec16<T>::N);
+  const int rows_per_block = half_warp ? 16 : 8;
+  const long long want = (M + rows_per_block - 1) / rows_per_block;
+  const int cap = sm_count() * 8;
+  const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
+  const T* xx = static_cast<const T*>(x);
+  const T* gg = static_cast<const T*>(gamma);
+  const T* bb = static_cast<const T*>(beta);
+  T* yy = static_cast<T*>(y);
+  auto k = half_warp ? layernorm_kernel<T, FPL, 16> : layernorm_kernel<T, FPL, 32>;
+  if (pdl) return launch_pdl(k, grid, dim3(256), 0, st, xx, gg, bb, yy, M, d, eps);
+  k<<<grid, 256, 0, st>>>(xx, gg, bb, yy, M, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm(la_dtype dt, const void* x, const void* gamma, const void* beta, void* y, long long M,
+                             int d, float eps, cudaStream_t st, bool pdl) {
+  if (M == 0) return cudaSuccess;
+  switch (dt) {
+    case LA_F32: return launch_ln<float, kLnFloatsPerLaneF32>(x, gamma, beta, y, M, d, eps, st, pdl);
+    case LA_BF16: return launch_ln<__nv_bfloat16, kLnFloatsPerLaneHalf>(x, gamma, beta, y, M, d, eps, st, pdl);
+    case LA_F16: return launch_ln<__half, kLnFloatsPerLaneHalf>(x, gamma, beta, y, M, d, eps, st, pdl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,

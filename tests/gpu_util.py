@@ -14,12 +14,12 @@ def need_gpu():
         pytest.skip("needs a CUDA GPU")
 
 
-def assert_close(got, want, dtype, what=""):
+def assert_close(got, want, dtype, what="", tol=None):
     g = got.detach().to(torch.float64).cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got)
     want = np.asarray(want, dtype=np.float64)
     assert g.shape == want.shape, (g.shape, want.shape)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
-    atol, rtol = TOL[dtype]
+    atol, rtol = TOL[dtype] if tol is None else tol
     err = np.abs(g - want)
     bound = atol + rtol * np.abs(want)
     ratio = err / bound

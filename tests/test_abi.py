@@ -161,3 +161,31 @@ def test_out_proj_workspace_sizes(lib):
     assert lib.la_workspace_size(api.LA_OP_OUT_PROJ, 1, 8, 4096, 4096, 64, api.LA_BF16) == 0
     bf = lib.la_workspace_size(api.LA_OP_LAYER_ATTN_OUT, 8, 8, 512, 512, 64, api.LA_BF16)
     assert bf == lib.la_workspace_size(api.LA_OP_LAYER_ATTN, 8, 8, 512, 512, 64, api.LA_BF16) + 8 * 512 * 512 * 2
+
+
+def test_layernorm_rejects_bad_arguments(lib):
+    def call(x=FAKE, g=FAKE, b=FAKE, y=FAKE, M=16, d=512, eps=1e-5, dt=api.LA_F32):
+        return lib.la_layernorm(x, g, b, y, M, d, eps, dt, None)
+    assert call(x=None) == api.LA_ERR_INVALID
+    assert call(g=None) == api.LA_ERR_INVALID
+    assert call(b=None) == api.LA_ERR_INVALID
+    assert call(M=-1) == api.LA_ERR_INVALID
+    assert call(eps=-1.0) == api.LA_ERR_INVALID
+    assert call(eps=float("nan")) == api.LA_ERR_INVALID
+    assert call(dt=9) == api.LA_ERR_INVALID
+    assert call(d=96) == api.LA_ERR_UNSUPPORTED
+    assert call(g=ctypes.c_void_p(0x7f0000000008)) == api.LA_ERR_INVALID
+    assert call(M=0) == api.LA_OK
+
+
+def test_layer_attn_ln_checks_arguments_before_launch(lib):
+    need = api.workspace_size(api.LA_OP_LAYER_ATTN_LN, 8, 8, 512, 512, 64, api.torch.float32)
+    assert need == api.workspace_size(api.LA_OP_LAYER_ATTN_OUT, 8, 8, 512, 512, 64, api.torch.float32) \
+        + 8 * 512 * 512 * 4                                       # + the normalised x
+    def call(g=FAKE, eps=1e-5, Wo=FAKE, bo=None, nb=need - 1):
+        return lib.la_layer_attn_ln(FAKE, g, FAKE, eps, FAKE, None, Wo, bo, FAKE, 8, 512, 512, 8, 0, None,
+                                    api.LA_F32, FAKE, nb, None)
+    assert call() == api.LA_ERR_WORKSPACE
+    assert call(g=None, nb=need) == api.LA_ERR_INVALID
+    assert call(eps=-0.5, nb=need) == api.LA_ERR_INVALID
+    assert call(Wo=None, bo=FAKE, nb=need) == api.LA_ERR_INVALID   # a bias without a weight
