@@ -326,6 +326,27 @@ uint32_t la_last_error_detail(void);
  */
 la_status la_debug_inject_timeout(int mode);
 
+/*
+ * The checked build: liblayerattn_checked.so is the same library compiled
+ * with bounds checks on every global store of the attention, merge and
+ * projection kernels (each flat element index against its buffer's extent).
+ * A store that would leave its buffer is skipped and the next
+ * la_get_last_error() returns LA_ERR_INTERNAL; nothing faults.  For
+ * debugging and tests; slower.  la_is_checked_build() returns 1 there, 0 in
+ * liblayerattn.so.
+ */
+int la_is_checked_build(void);
+
+/*
+ * Test hook for the checked build (the pages have no counterpart).  mode 1:
+ * the next attention launch declares its output buffer one row (D elements)
+ * shorter than it is, so the checked build skips the stores of the last row
+ * and reports LA_ERR_INTERNAL; the normal build ignores extents and writes
+ * every row.  mode 0 withdraws a pending request.  Returns LA_OK, or
+ * LA_ERR_INVALID for another mode.
+ */
+la_status la_debug_shrink_output_extent(int mode);
+
 /* Static, human-readable name of a status. */
 const char *la_status_string(la_status s);
 

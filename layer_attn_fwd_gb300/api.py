@@ -18,6 +18,8 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "liblayerattn.so")
+# the same library with bounds checks on every global store (see layerattn.h)
+CHECKED_LIB_PATH = os.path.join(_PKG, "_build", "liblayerattn_checked.so")
 
 LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_INTERNAL = range(7)
 LA_F32, LA_BF16, LA_F16 = 0, 1, 2
@@ -41,11 +43,12 @@ class la_kv_cache(ctypes.Structure):
                 ("D", ctypes.c_int), ("S_max", ctypes.c_int), ("len", ctypes.c_int), ("dtype", ctypes.c_int)]
 
 
-def load(path: str | None = None):
-    """Load the library (once).  Raises if it has not been built."""
+def load(path: str | None = None, reload: bool = False):
+    """Load the library (once; with reload, switch to `path`, e.g.
+    CHECKED_LIB_PATH).  Raises if it has not been built."""
     global _lib
     with _lock:
-        if _lib is not None:
+        if _lib is not None and not reload:
             return _lib
         path = path or LIB_PATH
         if not os.path.exists(path):
@@ -69,6 +72,10 @@ def load(path: str | None = None):
         lib.la_last_error_detail.restype = ctypes.c_uint32
         lib.la_debug_inject_timeout.argtypes = [I]
         lib.la_debug_inject_timeout.restype = I
+        lib.la_debug_shrink_output_extent.argtypes = [I]
+        lib.la_debug_shrink_output_extent.restype = I
+        lib.la_is_checked_build.argtypes = []
+        lib.la_is_checked_build.restype = I
         lib.la_status_string.argtypes = [I]
         lib.la_status_string.restype = ctypes.c_char_p
         for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_out_proj",
@@ -330,6 +337,17 @@ class Graph:
 def last_error_detail() -> int:
     """Raw device error word seen by the latest get_last_error()."""
     return int(load().la_last_error_detail())
+
+
+def is_checked_build() -> bool:
+    """True when the loaded library is the checked build."""
+    return bool(load().la_is_checked_build())
+
+
+def debug_shrink_output_extent(mode=1):
+    """Test hook: the next attention launch declares its output one row short,
+    so the checked build skips that row and reports LA_ERR_INTERNAL."""
+    _check(load().la_debug_shrink_output_extent(int(mode)), "la_debug_shrink_output_extent")
 
 
 def debug_inject_timeout(mode=1):

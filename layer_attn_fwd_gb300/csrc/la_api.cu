@@ -55,6 +55,8 @@ constexpr int kMaxDevices = 64;
 
 // One-shot request from la_debug_inject_timeout().
 std::atomic<int> g_skip_loads_once{0};
+// One-shot request from la_debug_shrink_output_extent().
+std::atomic<int> g_shrink_once{0};
 // Raw device error word seen by the latest la_get_last_error().
 std::atomic<uint32_t> g_last_word{0};
 
@@ -277,10 +279,20 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
   a.tiles_per_split = p.tiles_per_split;
   a.err = err;
   a.skip_loads = g_skip_loads_once.exchange(0);
+#if LA_CHECKED
+  // extents for the bounds checks: [B, H, S_q, D] elements either layout
+  a.o_elems = static_cast<long long>(B) * H * S_q * D;
+  if (g_shrink_once.exchange(0)) a.o_elems -= D;  // test hook: declare the last row outside
+#else
+  g_shrink_once.store(0);  // nothing is checked here: the hook has no effect
+#endif
   if (p.splits > 1) {
     const size_t rows = static_cast<size_t>(p.splits) * B * H * S_q;
     a.part_o = reinterpret_cast<float*>(w);
     a.part_lse = reinterpret_cast<float*>(w + round_up(rows * D * sizeof(float), 256));
+#if LA_CHECKED
+    a.part_elems = static_cast<long long>(rows) * D;
+#endif
   }
   cudaError_t e = launch_attn(dt, D, tq, tk, tv, a, p.splits, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
@@ -297,6 +309,10 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
     c.S_q = S_q;
     c.D = D;
     c.splits = p.splits;
+#if LA_CHECKED
+    c.o_elems = a.o_elems;
+    c.err = err;
+#endif
     e = launch_combine(dt, c, st);
     if (e != cudaSuccess) return LA_ERR_CUDA;
   }
@@ -364,6 +380,10 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   a.err = err;
   a.v_transposed = vt != nullptr;
   a.S_pad = vt_ld;
+#if LA_CHECKED
+  a.qk_elems = M * d_model;
+  a.v_elems = vt != nullptr ? static_cast<long long>(B) * d_model * vt_ld : M * d_model;
+#endif
   return cuda_status(launch_proj(dt, ps.block_n, tx, tw, a, st));
 }
 
@@ -398,6 +418,9 @@ la_status run_out_proj(const void* a_in, const void* Wo, const void* wot, const 
   a.D = d;
   a.q_scale = 1.f;
   a.err = err;
+#if LA_CHECKED
+  a.qk_elems = a.v_elems = M * d;
+#endif
   return cuda_status(launch_proj(dt, ps.block_n, tx, tw, a, st));
 }
 
@@ -724,6 +747,14 @@ la_status la_get_last_error(la_stream_t st) {
 }
 
 uint32_t la_last_error_detail(void) { return g_last_word.load(); }
+
+la_status la_debug_shrink_output_extent(int mode) {
+  if (mode != 0 && mode != 1) return LA_ERR_INVALID;
+  g_shrink_once.store(mode);
+  return LA_OK;
+}
+
+int la_is_checked_build(void) { return LA_CHECKED; }
 
 la_status la_debug_inject_timeout(int mode) {
   if (mode != 0 && mode != 1) return LA_ERR_INVALID;

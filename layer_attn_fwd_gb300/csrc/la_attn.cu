@@ -821,16 +821,18 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
             float v[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = u2f(o[c]) * inv;
-            if (row_ok) store_out32<float>(prow + c0, v);
+            if (row_ok && LA_IN_BOUNDS(prow - a.part_o + c0, 32, a.part_elems, a.err))
+              store_out32<float>(prow + c0, v);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&o_free[t]);
         } else if (row_ok) {
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c0 = 0; c0 < D; c0 += 4) *reinterpret_cast<float4*>(prow + c0) = z;
+          for (int c0 = 0; c0 < D; c0 += 4)
+            if (LA_IN_BOUNDS(prow - a.part_o + c0, 4, a.part_elems, a.err)) *reinterpret_cast<float4*>(prow + c0) = z;
         }
-        if (row_ok)
+        if (row_ok && LA_IN_BOUNDS((prow - a.part_o) / D, 1, a.part_elems / D, a.err))
           a.part_lse[(static_cast<size_t>(w.split) * a.B * a.H + w.bh) * a.S_q + q_row] =
               l > 0.f ? m_run + __log2f(l) : -INFINITY;
       } else if (has_o) {
@@ -871,7 +873,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int rr = r0 + 4 * i + sub;
-            if (rr < a.S_q) *reinterpret_cast<uint4*>(dst + static_cast<long long>(rr) * a.o_ss + c0) = wv[i];
+            if (rr < a.S_q && LA_IN_BOUNDS(dst - reinterpret_cast<T*>(a.o) + static_cast<long long>(rr) * a.o_ss + c0,
+                                           C::CW / 8, a.o_elems, a.err))
+              *reinterpret_cast<uint4*>(dst + static_cast<long long>(rr) * a.o_ss + c0) = wv[i];
           }
         }
       } else {
@@ -882,7 +886,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         for (int c = 0; c < 32; ++c) v[c] = 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32)
-          if (row_ok) store_out32<T>(dst + c0, v);
+          if (row_ok && LA_IN_BOUNDS(dst - reinterpret_cast<T*>(a.o) + c0, 32, a.o_elems, a.err))
+            store_out32<T>(dst + c0, v);
       }
       if (next < 0) break;
       idx = next;

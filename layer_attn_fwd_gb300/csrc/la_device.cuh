@@ -19,6 +19,29 @@ enum : uint32_t { DEVERR_TIMEOUT = 1u, DEVERR_INTERNAL = 2u };
 // the GB300's clocks), latches DEVERR_TIMEOUT and tells the whole CTA to stop.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// Checked build (compiled with -DLA_CHECKED=1 into a library of its own):
+// every global store's flat element index is compared with its buffer's
+// extent first; a store that would leave the buffer is skipped and
+// DEVERR_INTERNAL latched, so the call reports LA_ERR_INTERNAL instead of
+// touching memory it does not own.  In the normal build LA_IN_BOUNDS is the
+// constant true and its arguments are not even evaluated.
+#ifndef LA_CHECKED
+#define LA_CHECKED 0
+#endif
+#if LA_CHECKED
+__device__ __forceinline__ bool in_bounds(long long idx, long long width, long long extent, uint32_t* err) {
+  if (idx < 0 || idx + width > extent) {
+    atomicOr(err, DEVERR_INTERNAL);
+    return false;
+  }
+  return true;
+}
+// the arguments are evaluated in the checked build only
+#define LA_IN_BOUNDS(idx, width, extent, err) la::in_bounds((idx), (width), (extent), (err))
+#else
+#define LA_IN_BOUNDS(idx, width, extent, err) true
+#endif
+
 struct Abort {
   uint32_t* err;           // global error word
   volatile int* flag;      // CTA-wide stop flag in shared memory

@@ -8,6 +8,12 @@
 
 #include "layerattn.h"
 
+// The checked build (-DLA_CHECKED=1) adds buffer extents to the kernel
+// arguments and bounds checks to every global store (la_device.cuh).
+#ifndef LA_CHECKED
+#define LA_CHECKED 0
+#endif
+
 namespace la {
 
 // Launch with programmatic stream serialization: the grid may be scheduled
@@ -48,6 +54,10 @@ struct AttnArgs {
   unsigned long long* sched;  // work-item ticket counter and done count (set by the launcher)
   uint32_t* err;              // device error word
   int skip_loads;             // test hook: issue no TMA load, so every wait runs out
+#if LA_CHECKED
+  long long o_elems;          // elements of the output buffer
+  long long part_elems;       // elements of part_o (part_lse holds part_elems / D)
+#endif
 };
 
 // Static launch shape of the attention kernel for a dtype and head dim.
@@ -78,6 +88,10 @@ struct CombineArgs {
   void* o;
   long long o_sb, o_sh, o_ss;
   int B, H, S_q, D, splits;
+#if LA_CHECKED
+  long long o_elems;  // elements of o
+  uint32_t* err;      // device error word
+#endif
 };
 cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st);
 
@@ -111,6 +125,10 @@ struct ProjArgs {
   uint32_t* err;
   int v_transposed;   // write V as V^T [B, H, D, S_pad] (fp32 sublayer) instead of [B, H, S, D]
   long long S_pad;    // row length of V^T
+#if LA_CHECKED
+  long long qk_elems; // elements of each of q and k
+  long long v_elems;  // elements of v, or of V^T
+#endif
 };
 struct ProjShape {
   int block_n;        // output columns per tile (the wide tile or 128)

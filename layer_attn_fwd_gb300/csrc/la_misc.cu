@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     const long long i = row - bh * a.S_q;
     const long long b = bh / a.H, h = bh - b * a.H;
     T* dst = reinterpret_cast<T*>(a.o) + b * a.o_sb + h * a.o_sh + i * a.o_ss + c;
-    store4(dst, x0 * inv, x1 * inv, x2 * inv, x3 * inv);
+    if (LA_IN_BOUNDS(dst - reinterpret_cast<T*>(a.o), 4, a.o_elems, a.err)) store4(dst, x0 * inv, x1 * inv, x2 * inv, x3 * inv);
   }
 }
 

@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
             T* out =
                 reinterpret_cast<T*>(a.v) + ((static_cast<long long>(bidx) * a.H + hh) * a.D + dd) * a.S_pad + srow;
 #pragma unroll
-            for (int c = 0; c < CW; ++c) out[c * a.S_pad] = static_cast<T>(v[c]);
+            for (int c = 0; c < CW; ++c)
+              if (LA_IN_BOUNDS(out - reinterpret_cast<T*>(a.v) + c * a.S_pad, 1, a.v_elems, a.err))
+                out[c * a.S_pad] = static_cast<T>(v[c]);
           }
         } else {
           // row `lane` of the buffer, 16-byte unit u at u ^ lane%8 (conflict-free both ways)
@@ -325,7 +327,9 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (rok[i]) *reinterpret_cast<uint4*>(out + ro[i]) = w[i];
+            if (rok[i] && LA_IN_BOUNDS(out - reinterpret_cast<T*>(which == 0 ? a.q : (which == 1 ? a.k : a.v)) + ro[i],
+                                       16 / C::E, which == 2 ? a.v_elems : a.qk_elems, a.err))
+              *reinterpret_cast<uint4*>(out + ro[i]) = w[i];
         }
       }
       tc_fence_before();

@@ -189,3 +189,16 @@ def test_layer_attn_ln_checks_arguments_before_launch(lib):
     assert call(g=None, nb=need) == api.LA_ERR_INVALID
     assert call(eps=-0.5, nb=need) == api.LA_ERR_INVALID
     assert call(Wo=None, bo=FAKE, nb=need) == api.LA_ERR_INVALID   # a bias without a weight
+
+
+def test_checked_build_exports_and_identifies_itself(lib):
+    """liblayerattn_checked.so (bounds checks on every global store) exports
+    the same entry points; each library says which it is."""
+    checked = ctypes.CDLL(build.LIB_CHECKED)
+    for n in _declared():
+        assert hasattr(checked, n), n
+    checked.la_is_checked_build.restype = ctypes.c_int
+    assert checked.la_is_checked_build() == 1
+    assert lib.la_is_checked_build() == 0
+    assert lib.la_debug_shrink_output_extent(3) == api.LA_ERR_INVALID
+    assert lib.la_debug_shrink_output_extent(0) == api.LA_OK

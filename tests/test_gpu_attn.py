@@ -142,23 +142,29 @@ def _sampled(o, rows):
     return o[r[:, 0], r[:, 1], r[:, 2]]
 
 
+# The workloads over 8 seeds each (inputs and sampled rows both seeded).
+WORKLOAD_SEEDS = range(8)
+
+
 @pytest.mark.parametrize("padded", [False, True])
-def test_workload_fp32_causal_2048(padded):
+@pytest.mark.parametrize("seed", WORKLOAD_SEEDS)
+def test_workload_fp32_causal_2048(padded, seed):
     """fp32 causal B=8 H=8 S=2048 D=64 (and the padded variant), 512 sampled rows."""
     B, H, S, D = 8, 8, 2048, 64
-    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=21)
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=21 + 100 * seed)
     kv_len = inputs.padding_kv_len(B, S) if padded else None
     o = _gpu_attn(q, k, v, True, kv_len=kv_len).cpu()
-    rows = inputs.sample_rows(B, H, S, n=512, seed=22, forced=(0, 127, 128, 1535, 1536, 2047))
+    rows = inputs.sample_rows(B, H, S, n=512, seed=22 + 100 * seed, forced=(0, 127, 128, 1535, 1536, 2047))
     want = oracle.attn_rows(q, k, v, rows, causal=True, kv_len=kv_len)
-    assert_close(_sampled(o, rows), want, torch.float32, "fp32 causal 2048")
+    assert_close(_sampled(o, rows), want, torch.float32, f"fp32 causal 2048, seed {seed}")
 
 
-def test_workload_bf16_causal_4096():
+@pytest.mark.parametrize("seed", WORKLOAD_SEEDS)
+def test_workload_bf16_causal_4096(seed):
     """bf16 causal B=4 H=16 S=4096 D=128, 256 sampled rows."""
     B, H, S, D = 4, 16, 4096, 128
-    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=31)
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=31 + 100 * seed)
     o = _gpu_attn(q, k, v, True).cpu()
-    rows = inputs.sample_rows(B, H, S, n=256, seed=32, forced=(0, 255, 256, 4095))
+    rows = inputs.sample_rows(B, H, S, n=256, seed=32 + 100 * seed, forced=(0, 255, 256, 4095))
     want = oracle.attn_rows(q, k, v, rows, causal=True)
-    assert_close(_sampled(o, rows), want, torch.bfloat16, "bf16 causal 4096")
+    assert_close(_sampled(o, rows), want, torch.bfloat16, f"bf16 causal 4096, seed {seed}")

@@ -47,9 +47,10 @@ def test_qkv_proj_no_bias():
         assert_close(got, want, torch.bfloat16)
 
 
-def test_layer_fp32_b8_s512_d512():
-    """The attention sublayer workload: fp32 x [8,512,512], Wqkv ~ N(0,1/512), zero bias, H=8."""
-    x, W, b = inputs.layer_inputs(8, 512, 512, torch.float32, seed=43)
+@pytest.mark.parametrize("seed", range(8))
+def test_layer_fp32_b8_s512_d512(seed):
+    """The attention sublayer workload: fp32 x [8,512,512], Wqkv ~ N(0,1/512), zero bias, H=8; 8 seeds."""
+    x, W, b = inputs.layer_inputs(8, 512, 512, torch.float32, seed=43 + 100 * seed)
     o = api.layer_attn(x.cuda(), W.cuda(), b.cuda(), 8)
     assert api.get_last_error() == api.LA_OK
     assert_close(o, oracle.layer_attn(x, W, b, 8), torch.float32, "layer")
