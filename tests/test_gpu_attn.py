@@ -159,6 +159,17 @@ def test_workload_fp32_causal_2048(padded, seed):
     assert_close(_sampled(o, rows), want, torch.float32, f"fp32 causal 2048, seed {seed}")
 
 
+@pytest.mark.parametrize("seed", range(2))
+def test_workload_f16_causal_4096(seed):
+    """The same workload in fp16 (the fp16 configuration), 256 sampled rows."""
+    B, H, S, D = 4, 16, 4096, 128
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float16, seed=41 + 100 * seed)
+    o = _gpu_attn(q, k, v, True).cpu()
+    rows = inputs.sample_rows(B, H, S, n=256, seed=42 + 100 * seed, forced=(0, 255, 256, 4095))
+    want = oracle.attn_rows(q, k, v, rows, causal=True)
+    assert_close(_sampled(o, rows), want, torch.float16, f"f16 causal 4096, seed {seed}")
+
+
 @pytest.mark.parametrize("seed", WORKLOAD_SEEDS)
 def test_workload_bf16_causal_4096(seed):
     """bf16 causal B=4 H=16 S=4096 D=128, 256 sampled rows."""
