@@ -110,6 +110,30 @@ def _dt(t):
         raise TypeError(f"unsupported dtype {t.dtype}") from None
 
 
+def _spec(t, name, shape=None, dtype=None):
+    """t: a tensor of exactly `shape` and `dtype` (None: not checked).  The
+    library takes plain pointers and cannot see a tensor's size, so every
+    entry point checks each operand's shape and type here, before anything
+    touches a device: a short weight or a wider element type would make a
+    kernel read past a buffer."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _spec_opt(t, name, shape, dtype):
+    if t is not None:
+        _spec(t, name, shape, dtype)
+
+
+def _kvlen_spec(kv_len, B):
+    if kv_len is not None:
+        _spec(kv_len, "kv_len", (B,), torch.int32)
+
+
 def _need(t, name, dev=True):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -136,12 +160,20 @@ def _workspace(nbytes, device, ws):
 
 def qkv_proj(x, Wqkv, bqkv, H, q_scale=1.0, out=None, workspace=None, stream=None):
     """x [B,S,d], Wqkv [d,3d], bqkv [3d] or None -> q, k, v [B,H,S,D]."""
+    _spec(x, "x")
+    if x.dim() != 3:
+        raise ValueError("x must be [B, S, d_model]")
+    B, S, dm = x.shape
+    D = dm // H if H > 0 else 0
+    _spec(Wqkv, "Wqkv", (dm, 3 * dm), x.dtype)
+    _spec_opt(bqkv, "bqkv", (3 * dm,), x.dtype)
+    if out is not None:
+        for t, n in zip(out, "qkv"):
+            _spec(t, n, (B, H, S, D), x.dtype)
     for t, n in ((x, "x"), (Wqkv, "Wqkv")):
         _need(t, n)
     if bqkv is not None:
         _need(bqkv, "bqkv")
-    B, S, dm = x.shape
-    D = dm // H if H > 0 else 0
     if out is None:
         out = tuple(torch.empty(B, H, S, D, dtype=x.dtype, device=x.device) for _ in range(3))
     q, k, v = out
@@ -160,19 +192,30 @@ def fp32_vt_bytes(B, H, S_kv, D):
     return (n + 255) // 256 * 256
 
 
+def _attn_spec(q, k, v, kv_len, out):
+    _spec(q, "q")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S_q, D]")
+    B, H, S_q, D = q.shape
+    _spec(k, "k", None, q.dtype)
+    if k.dim() != 4:
+        raise ValueError("k must be [B, H, S_kv, D]")
+    S_kv = k.shape[2]
+    _spec(k, "k", (B, H, S_kv, D), q.dtype)
+    _spec(v, "v", (B, H, S_kv, D), q.dtype)
+    _kvlen_spec(kv_len, B)
+    _spec_opt(out, "out", (B, H, S_q, D), q.dtype)
+    return B, H, S_q, D, S_kv
+
+
 def attn_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, workspace=None, stream=None):
     """softmax(scale q k^T) v: q [B,H,S_q,D], k/v [B,H,S_kv,D] -> [B,H,S_q,D]."""
+    B, H, S_q, D, S_kv = _attn_spec(q, k, v, kv_len, out)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n)
-    B, H, S_q, D = q.shape
-    S_kv = k.shape[2]
-    if k.shape != (B, H, S_kv, D) or v.shape != k.shape:
-        raise ValueError("k and v must be [B,H,S_kv,D] matching q")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if kv_len is not None:
         _need(kv_len, "kv_len")
-        if kv_len.dtype != torch.int32 or kv_len.shape != (B,):
-            raise ValueError("kv_len must be int32 [B]")
     o = torch.empty_like(q) if out is None else out
     if workspace is None and D in (64, 128) and q.dtype in _DT:
         workspace = _workspace(workspace_size(LA_OP_ATTN_FWD, B, H, S_q, S_kv, D, q.dtype), q.device, None)
@@ -185,12 +228,11 @@ def attn_fwd(q, k, v, causal=False, scale=None, kv_len=None, out=None, workspace
 def attn_fwd_noalloc(q, k, v, causal=False, scale=None, kv_len=None, out=None, stream=None):
     """attn_fwd for callers that cannot allocate: the library's own static
     16 MiB device scratch stands in for the workspace (see layerattn.h)."""
+    B, H, S_q, D, S_kv = _attn_spec(q, k, v, kv_len, out)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n)
-    B, H, S_q, D = q.shape
-    S_kv = k.shape[2]
-    if k.shape != (B, H, S_kv, D) or v.shape != k.shape:
-        raise ValueError("k and v must be [B,H,S_kv,D] matching q")
+    if kv_len is not None:
+        _need(kv_len, "kv_len")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     _check(load().la_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S_q, S_kv, D, int(bool(causal)),
@@ -217,6 +259,15 @@ class KVCache:
 def attn_chunked(q_chunk, k_chunk, v_chunk, cache: KVCache, causal=True, scale=None, out=None, workspace=None,
                  stream=None):
     """Append this window's k/v to the cache, then attend q_chunk to the cache."""
+    c = cache.c
+    dtype = cache.k.dtype
+    _spec(q_chunk, "q_chunk", None, dtype)
+    if q_chunk.dim() != 4:
+        raise ValueError("q_chunk must be [B, H, chunk, D]")
+    shape = (c.B, c.H, q_chunk.shape[2], c.D)
+    for t, n in ((q_chunk, "q_chunk"), (k_chunk, "k_chunk"), (v_chunk, "v_chunk")):
+        _spec(t, n, shape, dtype)
+    _spec_opt(out, "out", shape, dtype)
     for t, n in ((q_chunk, "q_chunk"), (k_chunk, "k_chunk"), (v_chunk, "v_chunk")):
         _need(t, n)
     B, H, C, D = q_chunk.shape
@@ -232,11 +283,22 @@ def attn_chunked(q_chunk, k_chunk, v_chunk, cache: KVCache, causal=True, scale=N
     return o
 
 
+def _layer_spec(x, Wqkv, bqkv, H, kv_len, out):
+    _spec(x, "x")
+    if x.dim() != 3:
+        raise ValueError("x must be [B, S, d_model]")
+    B, S, dm = x.shape
+    _spec(Wqkv, "Wqkv", (dm, 3 * dm), x.dtype)
+    _spec_opt(bqkv, "bqkv", (3 * dm,), x.dtype)
+    _kvlen_spec(kv_len, B)
+    _spec_opt(out, "out", (B, S, dm), x.dtype)
+    return B, S, dm, (dm // H if H > 0 else 0)
+
+
 def layer_attn(x, Wqkv, bqkv, H, causal=False, kv_len=None, out=None, workspace=None, stream=None):
     """Projection + per-head attention + head merge: x [B,S,d] -> [B,S,d]."""
+    B, S, dm, D = _layer_spec(x, Wqkv, bqkv, H, kv_len, out)
     _need(x, "x")
-    B, S, dm = x.shape
-    D = dm // H if H > 0 else 0
     o = torch.empty_like(x) if out is None else out
     if workspace is None:
         workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN, B, H, S, S, D, x.dtype), x.device, None)
@@ -248,11 +310,15 @@ def layer_attn(x, Wqkv, bqkv, H, causal=False, kv_len=None, out=None, workspace=
 
 def out_proj(a, Wo, bo=None, out=None, workspace=None, stream=None):
     """a [..., d] (row-major), Wo [d, d], bo [d] or None -> a Wo + bo."""
+    _spec(a, "a")
+    dm = a.shape[-1] if a.dim() > 0 else 0
+    _spec(Wo, "Wo", (dm, dm), a.dtype)
+    _spec_opt(bo, "bo", (dm,), a.dtype)
+    _spec_opt(out, "out", tuple(a.shape), a.dtype)
     for t, n in ((a, "a"), (Wo, "Wo")):
         _need(t, n)
     if bo is not None:
         _need(bo, "bo")
-    dm = a.shape[-1]
     M = a.numel() // dm if dm > 0 else 0
     y = torch.empty_like(a) if out is None else out
     if workspace is None and dm % 64 == 0 and dm > 0 and a.dtype in _DT:
@@ -265,9 +331,10 @@ def out_proj(a, Wo, bo=None, out=None, workspace=None, stream=None):
 
 def layer_attn_out(x, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=None, out=None, workspace=None, stream=None):
     """The sublayer with its output projection: x [B,S,d] -> [B,S,d]."""
+    B, S, dm, D = _layer_spec(x, Wqkv, bqkv, H, kv_len, out)
+    _spec(Wo, "Wo", (dm, dm), x.dtype)
+    _spec_opt(bo, "bo", (dm,), x.dtype)
     _need(x, "x")
-    B, S, dm = x.shape
-    D = dm // H if H > 0 else 0
     y = torch.empty_like(x) if out is None else out
     if workspace is None:
         workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN_OUT, B, H, S, S, D, x.dtype), x.device, None)
@@ -280,9 +347,13 @@ def layer_attn_out(x, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=None, out=None
 
 def layernorm(x, gamma, beta, eps=1e-5, out=None, stream=None):
     """LayerNorm over the last dimension of x (rows of d, d a multiple of 64)."""
+    _spec(x, "x")
+    d = x.shape[-1] if x.dim() > 0 else 0
+    _spec(gamma, "gamma", (d,), x.dtype)
+    _spec(beta, "beta", (d,), x.dtype)
+    _spec_opt(out, "out", tuple(x.shape), x.dtype)
     for t, n in ((x, "x"), (gamma, "gamma"), (beta, "beta")):
         _need(t, n)
-    d = x.shape[-1]
     M = x.numel() // d if d > 0 else 0
     y = torch.empty_like(x) if out is None else out
     _check(load().la_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), M, d, float(eps), _dt(x),
@@ -294,9 +365,12 @@ def layer_attn_ln(x, gamma, beta, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=No
                   workspace=None, stream=None):
     """The pre-norm attention block: LayerNorm, the sublayer and (Wo not None)
     the output projection: x [B,S,d] -> [B,S,d]."""
+    B, S, dm, D = _layer_spec(x, Wqkv, bqkv, H, kv_len, out)
+    _spec(gamma, "gamma", (dm,), x.dtype)
+    _spec(beta, "beta", (dm,), x.dtype)
+    _spec_opt(Wo, "Wo", (dm, dm), x.dtype)
+    _spec_opt(bo, "bo", (dm,), x.dtype)
     _need(x, "x")
-    B, S, dm = x.shape
-    D = dm // H if H > 0 else 0
     y = torch.empty_like(x) if out is None else out
     if workspace is None:
         workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN_LN, B, H, S, S, D, x.dtype), x.device, None)
