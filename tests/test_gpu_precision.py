@@ -28,12 +28,12 @@ import torch
 
 import oracle
 from gpu_util import need_gpu
+from precision_bound import SLACK, rounding_bound
 from layer_attn_fwd_gb300 import api, build, inputs, ulp
 
 pytestmark = pytest.mark.gpu
 
 FMT = {torch.bfloat16: "bf16", torch.float16: "f16"}
-SLACK = 2.0 ** -12
 _study = {}
 
 
@@ -49,14 +49,7 @@ def _lib():
             json.dump(_study, f, indent=1)
 
 
-def _bound(r, g, P, v, fmt):
-    """Per-element bound of the two roundings (see the module docstring)."""
-    av = np.abs(v)
-    ep = np.einsum("bhij,bhjd->bhid", P, av)                 # sum_j p_j |v_j|
-    b = 0.5 * np.maximum(ulp.ulp(r, fmt), ulp.ulp(g, fmt)) + ulp.unit_roundoff(fmt) * ep
-    if fmt == "f16":
-        b += 2.0 ** -25 * np.einsum("bhij,bhjd->bhid", (P > 0).astype(np.float64), av)
-    return b + SLACK * (ep + np.abs(r))
+_bound = rounding_bound
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
