@@ -149,8 +149,38 @@ class Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         load = [s for s in sm if mx and s > 0.5 * mx] or sm
-        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows)}
+        med = statistics.median(load) if load else None
+        # a run counts only if no slowdown reason was active and the clock held
+        # at least 85% of its maximum (sw_power_cap is normal under load)
+        bad = [r for r in reasons if r != "sw_power_cap"]
+        ok = not bad and med is not None and mx is not None and med >= 0.85 * mx
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows), "ok": ok}
+
+
+def _commit():
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "--short", "HEAD"], capture_output=True, text=True,
+                           timeout=10)
+        if r.returncode != 0:
+            return None
+        dirty = subprocess.run(["git", "-C", ROOT, "status", "--porcelain", "--untracked-files=no"],
+                               capture_output=True, text=True, timeout=10).stdout.strip()
+        return r.stdout.strip() + ("+dirty" if dirty else "")
+    except Exception:
+        return None
+
+
+def emit(line, log_path=None):
+    """Print the bench line; with a log path also append it, with the commit
+    it ran from, to that append-only JSON-lines file."""
+    text = json.dumps(line)
+    print(text, flush=True)
+    if log_path:
+        rec = dict(line)
+        rec["commit"] = _commit()
+        rec["logged_at"] = time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime())
+        with open(log_path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
 
 
 def max_over_ranks(x, dist=None, device="cpu"):
@@ -321,7 +351,7 @@ def run_ours(args):
             "gpu_launches": launches_per_step * K, "clocks": clocks, "cpu_baseline": cpu,
             "workloads": workloads, "peaks": peaks,
         }
-        print(json.dumps(line), flush=True)
+        emit(line, args.log)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -586,7 +616,7 @@ def run_reference(args):
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line, args.log)
 
 
 def main():
@@ -598,6 +628,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--log", metavar="PATH", help="also append the line, with the commit it ran from, to PATH "
+                                                  "(JSON lines)")
     ap.add_argument("--only", choices=["fp32-causal-2048", "fp32-causal-2048-padded", "bf16-causal-4096",
                                        "fp32-small", "small-graph", "layer-out-fp32", "layer-out-bf16", "layer-out-f16",
                                        "chunked-100k"],
