@@ -192,6 +192,19 @@ def max_over_ranks(x, dist=None, device="cpu"):
     return float(t.item())
 
 
+# Before each timed step the stream spins this many SM cycles (after the L2
+# flush, outside the events), so that the host has enqueued the whole step
+# before its first kernel starts: the events then see device time only, not
+# the host's argument checks and launch calls.
+SPIN_CYCLES = 200_000
+
+
+def _pre_step(flush, stream):
+    with torch.cuda.stream(stream):
+        flush.zero_()
+        torch.cuda._sleep(SPIN_CYCLES)
+
+
 def _time_steps(step, K, W, flush, stream, barrier):
     """W untimed steps, then K steps each bracketed by CUDA events on `stream`
     with an L2 flush (not timed) between them.  Returns total device ms."""
@@ -203,7 +216,7 @@ def _time_steps(step, K, W, flush, stream, barrier):
     evs = []
     with torch.cuda.stream(stream):
         for _ in range(K):
-            flush.zero_()
+            _pre_step(flush, stream)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             step()
@@ -213,6 +226,34 @@ def _time_steps(step, K, W, flush, stream, barrier):
     barrier()
     torch.cuda.synchronize()
     return sum(s.elapsed_time(e) for s, e in evs)
+
+
+def kernel_times(api, step, K, flush, stream):
+    """Device time of each kernel of a step, each launch bracketed by CUDA
+    events on its own stream by the library (la_profile_start): K steps with
+    an L2 flush before each; per kernel name the median over steps of its
+    summed launch times, and its launches per step."""
+    torch.cuda.synchronize()
+    with api.Profile(max_launches=256 * K) as prof:
+        for _ in range(K):
+            _pre_step(flush, stream)
+            step()
+    torch.cuda.synchronize()
+    recs = prof.records
+    if not recs or len(recs) % K or len(recs) >= 256 * K:  # (a full record buffer would drop launches)
+        return {}
+    per = len(recs) // K
+    out = {}
+    for i in range(K):
+        step_sum = {}
+        for name, ms in recs[i * per:(i + 1) * per]:
+            step_sum[name] = step_sum.get(name, 0.0) + ms
+        for name, ms in step_sum.items():
+            out.setdefault(name, []).append(ms)
+    launches = {}
+    for name, _ in recs[:per]:
+        launches[name] = launches.get(name, 0) + 1
+    return {name: {"ms": statistics.median(v), "launches_per_step": launches[name]} for name, v in out.items()}
 
 
 # ---------------------------------------------------------------------------
@@ -242,7 +283,8 @@ def run_ours(args):
 
     if args.only:
         # one named workload alone (for profiler captures of one kernel)
-        res = other_workloads(args, dev, stream, flush, barrier, peaks)
+        res = other_workloads(args, dev, stream, flush, barrier, peaks,
+                              cpu_ok=rank == 0 and ws_n == 1 and not args.no_cpu)
         if rank == 0:
             print(json.dumps({"only": args.only, "workloads": res}), flush=True)
         if dist is not None:
@@ -257,8 +299,6 @@ def run_ours(args):
     o = torch.empty_like(x)
     ws_layer = api.workspace_size(api.LA_OP_LAYER_ATTN, B, H, S, S, D, torch.float32)
     ws = torch.empty(ws_layer, dtype=torch.uint8, device=dev)
-    qkv_bytes = 3 * ((B * S * dm * 4 + 255) // 256 * 256)
-    launches_per_step = 2 + (1 if ws_layer > qkv_bytes else 0)
     fl_proj = flops.proj_flops(B, S, dm)
     fl_attn = flops.attn_flops(B, H, S, S, D, False)
     fl_step = fl_proj + fl_attn
@@ -276,27 +316,27 @@ def run_ours(args):
     ms_step = ms_max / K
     value = fl_step * K * ws_n / (ms_max * 1e-3) / 1e12
 
-    # ---- the two kernels of the step, each timed alone ------------------------
-    q = torch.empty(B, H, S, D, device=dev)
-    k = torch.empty_like(q)
-    v = torch.empty_like(q)
-    oh = torch.empty_like(q)
-    api.qkv_proj(x, Wq, bq, H, out=(q, k, v), stream=stream)
-    ms_proj = _time_steps(lambda: api.qkv_proj(x, Wq, bq, H, out=(q, k, v), stream=stream), K, W, flush, stream,
-                          barrier) / K
-    ms_att = _time_steps(lambda: api.attn_fwd(q, k, v, out=oh, stream=stream), K, W, flush, stream, barrier) / K
-    per_kernel = {
-        "qkv_proj": {"ms": ms_proj, "tflops": fl_proj / (ms_proj * 1e-3) / 1e12},
-        "attn_fwd": {"ms": ms_att, "tflops": fl_attn / (ms_att * 1e-3) / 1e12},
-    }
-    dom = "attn_fwd" if ms_att >= ms_proj else "qkv_proj"
+    # ---- each kernel of the step alone (events around every launch) -----------
+    kt = kernel_times(api, layer_step, K, flush, stream)
+    kernel_flops = {"qkv_proj_kernel": fl_proj, "attn_fwd_kernel": fl_attn}
+    per_kernel = {}
+    for name, t in kt.items():
+        e = {"ms": round(t["ms"], 5), "launches_per_step": t["launches_per_step"]}
+        if name in kernel_flops:
+            e["tflops"] = round(kernel_flops[name] / (t["ms"] * 1e-3) / 1e12, 2)
+        elif name == "transpose32_kernel":  # Wqkv^T, 3 d^2 fp32 read and written
+            e["gbs"] = round(2 * 3 * dm * dm * 4 / (t["ms"] * 1e-3) / 1e9, 1)
+        per_kernel[name] = e
+    dom = max((n for n in per_kernel if n in kernel_flops), key=lambda n: per_kernel[n]["ms"])
     peak_tf32 = _tensor_peak(torch.float32, peaks)
-    src = ["la_attn.cu", "la_device.cuh"] if dom == "attn_fwd" else ["la_proj.cu", "la_device.cuh"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(per_kernel[dom]["tflops"], 2),
+    src = ["la_attn.cu", "la_device.cuh"] if dom == "attn_fwd_kernel" else ["la_proj.cu", "la_device.cuh"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": per_kernel[dom]["tflops"],
                 "peak": round(peak_tf32, 1), "unit": "TFLOP/s",
                 "frac": round(per_kernel[dom]["tflops"] / peak_tf32, 4),
                 "traffic": _traffic(dom, "sublayer fp32 B8 S512 d512", src),
-                "peak_note": f"TF32 = {peaks['source']} bf16 burst x nominal 1.1/2.25"}
+                "algorithmic": f"{kernel_flops[dom] / 1e9:.3f} GFLOP per launch",
+                "timing": "CUDA events around each launch on its stream (la_profile_start), median of the steps",
+                "peak_note": f"TF32 = {peaks['source']} bf16 burst x nominal 1.1/2.25 (of measured)"}
 
     # ---- end to end through the public API, host buffers -------------------------
     # Serial: each step copies its input in, runs the sublayer and reads the
@@ -318,7 +358,13 @@ def run_ours(args):
     # and outputs rotate through 16 slots (134 MB each way, more than L2),
     # so no flush is needed.
     ms_pipe = max_over_ranks(e2e_pipelined(api, x_h, Wq, bq, H, ws, stream, dev, K, W, barrier), dist, dev)
+    link = link_peak(dev)
+    step_link_gbs = 2 * x_h.numel() * 4 / (ms_pipe / K * 1e-3) / 1e9
     e2e = {"value": round(fl_step * K * ws_n / (ms_pipe * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+           "link": {"achieved_gbs": round(step_link_gbs, 1), "peak_gbs": link["both_gbs"],
+                    "frac": round(step_link_gbs / link["both_gbs"], 4), "measured": link,
+                    "note": "the pipelined step's copies in and out (both directions at once) against the measured "
+                            "pinned copy bandwidth with both directions busy"},
            "ms_per_step": round(ms_pipe / K, 4), "h2d_bytes_per_step": x_h.numel() * 4,
            "d2h_bytes_per_step": x_h.numel() * 4,
            "pipeline": "input copy, sublayer and result read on three streams, step i's compute overlapping "
@@ -331,7 +377,8 @@ def run_ours(args):
     # ---- the other workloads of the path --------------------------------------------
     workloads = {}
     if not args.headline_only:
-        workloads = other_workloads(args, dev, stream, flush, barrier, peaks)
+        workloads = other_workloads(args, dev, stream, flush, barrier, peaks,
+                                    cpu_ok=rank == 0 and ws_n == 1 and not args.no_cpu)
 
     # ---- CPU baseline: the oracle on the host cores (rank 0, N=1 only) ------------------
     cpu = None
@@ -348,12 +395,57 @@ def run_ours(args):
                        "batch": B, "seq_len": S, "d_model": dm, "heads": H},
             "frac_of_tensor_peak": round(value / ws_n / peak_tf32, 4),
             "roofline": roofline, "per_kernel": per_kernel, "e2e": e2e,
-            "gpu_launches": launches_per_step * K, "clocks": clocks, "cpu_baseline": cpu,
+            "gpu_launches": sum(t["launches_per_step"] for t in kt.values()) * K, "clocks": clocks,
+            "cpu_baseline": cpu,
             "workloads": workloads, "peaks": peaks,
         }
         emit(line, args.log)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def link_peak(dev, nbytes=256 << 20, reps=5):
+    """Measured pinned host <-> device copy bandwidth (GB/s): host to device
+    alone, device to host alone, and both at once on two streams (best of
+    `reps`, CUDA events, 256 MB each way)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def best(fn):
+        t = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s1)
+            s2.wait_event(a)
+            fn()
+            s1.wait_stream(s2)
+            b.record(s1)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b))
+        return min(t)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = best(h2d), best(d2h), best(both)
+    res = {"h2d_gbs": round(nbytes / (t_in * 1e-3) / 1e9, 1), "d2h_gbs": round(nbytes / (t_out * 1e-3) / 1e9, 1),
+           "both_gbs": round(2 * nbytes / (t_both * 1e-3) / 1e9, 1),
+           "how": "256 MB pinned buffers, best of 5, CUDA events; both = the two directions at once on two streams"}
+    del h_in, h_out, d_in, d_out
+    return res
 
 
 def e2e_pipelined(api, x_h, Wq, bq, H, ws, stream, dev, K, W, barrier, slots=16, copy_streams=1):
@@ -408,7 +500,7 @@ def e2e_pipelined(api, x_h, Wq, bq, H, ws, stream, dev, K, W, barrier, slots=16,
     return start.elapsed_time(end)
 
 
-def other_workloads(args, dev, stream, flush, barrier, peaks):
+def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
     from layer_attn_fwd_gb300 import api, flops, inputs
 
     res = {}
@@ -417,29 +509,46 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
     def wanted(key):
         return not args.only or args.only == key
 
-    def attn_case(key, name, B, H, S, D, dt, causal, padded=False):
+    def attn_case(key, name, B, H, S, D, dt, causal, padded=False, small=False):
         if not wanted(key):
             return
-        q, k, v = (t.to(dev) for t in inputs.attn_inputs(B, H, S, S, D, dt, seed=0))
+        qh, kh, vh = inputs.attn_inputs(B, H, S, S, D, dt, seed=0)
+        q, k, v = (t.to(dev) for t in (qh, kh, vh))
         kv = inputs.padding_kv_len(B, S) if padded else None
         kl = kv.to(dev) if kv is not None else None
         o = torch.empty_like(q)
         n = api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, dt)
         ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
-        ms = _time_steps(lambda: api.attn_fwd(q, k, v, causal=causal, kv_len=kl, out=o, workspace=ws,
-                                              stream=stream), Kx, 3, flush, stream, barrier) / Kx
+
+        def step():
+            api.attn_fwd(q, k, v, causal=causal, kv_len=kl, out=o, workspace=ws, stream=stream)
+
+        ms = _time_steps(step, Kx, 3, flush, stream, barrier) / Kx
+        kt = kernel_times(api, step, Kx, flush, stream)
         fl = flops.attn_flops(B, H, S, S, D, causal, kv)
         tf = fl / (ms * 1e-3) / 1e12
         pk = _tensor_peak(dt, peaks)
-        res[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / pk, 4),
-                     "gflop": round(fl / 1e9, 3)}
+        ka = kt.get("attn_fwd_kernel", {}).get("ms")
+        r = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / pk, 4),
+             "gflop": round(fl / 1e9, 3),
+             "per_kernel_ms": {n_: round(t["ms"], 5) for n_, t in kt.items()}}
+        if ka:
+            r["attn_kernel"] = {"ms": round(ka, 5), "tflops": round(fl / (ka * 1e-3) / 1e12, 2),
+                                "frac_of_tensor_peak": round(fl / (ka * 1e-3) / 1e12 / pk, 4)}
+        if small:  # latency bound: also bytes moved (q, k, v read, o written once) against the copy bandwidth
+            nbytes = 4 * B * H * S * D * q.element_size()
+            r["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 2)
+            r["frac_of_hbm"] = round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)
+        if cpu_ok:
+            r["cpu_baseline"] = cpu_attn_baseline(qh, kh, vh, causal, kv, fl, full=small)
+        res[name] = r
         del q, k, v, o, ws
 
     attn_case("fp32-causal-2048", "fp32 causal B8 H8 S2048 D64", 8, 8, 2048, 64, torch.float32, True)
     attn_case("fp32-causal-2048-padded", "fp32 causal B8 H8 S2048 D64, last 25% keys padded for half the batch",
               8, 8, 2048, 64, torch.float32, True, padded=True)
     attn_case("bf16-causal-4096", "bf16 causal B4 H16 S4096 D128", 4, 16, 4096, 128, torch.bfloat16, True)
-    attn_case("fp32-small", "fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False)
+    attn_case("fp32-small", "fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False, small=True)
 
     def layer_out_case(key, name, dt):
         """The sublayer (la_layer_attn), the sublayer with its output projection
@@ -460,6 +569,16 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
                          Kx, 3, flush, stream, barrier) / Kx
         ms_ln = _time_steps(lambda: api.layer_attn_ln(x, gam, bet, Wq, bq, Wo, bo, H, out=y, workspace=ws,
                                                       stream=stream), Kx, 3, flush, stream, barrier) / Kx
+        # the same three forms on weights prepared once (la_prepare_weight), as a
+        # server runs them: no per-call conversion of the constant weights
+        Wqp, Wop = api.prepare_weight(Wq), api.prepare_weight(Wo)
+        ms_lp = _time_steps(lambda: api.layer_attn_prepared(x, Wqp, bq, H, out=y, workspace=ws, stream=stream),
+                            Kx, 3, flush, stream, barrier) / Kx
+        ms_op = _time_steps(lambda: api.layer_attn_prepared(x, Wqp, bq, H, Wo_p=Wop, bo=bo, out=y, workspace=ws,
+                                                            stream=stream), Kx, 3, flush, stream, barrier) / Kx
+        ms_lnp = _time_steps(lambda: api.layer_attn_prepared(x, Wqp, bq, H, gamma=gam, beta=bet, Wo_p=Wop, bo=bo,
+                                                             out=y, workspace=ws, stream=stream),
+                             Kx, 3, flush, stream, barrier) / Kx
         fl_l = flops.proj_flops(B, S, dm) + flops.attn_flops(B, H, S, S, dm // H, False)
         fl = fl_l + flops.out_proj_flops(B, S, dm)
         o = api.layer_attn(x, Wq, bq, H, stream=stream)
@@ -479,8 +598,15 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
                                        "note": "LayerNorm + sublayer + output projection"},
                      "out_proj": {"ms": round(ms_o, 4), "tflops": round(tf_o, 2),
                                   "frac_of_tensor_peak": round(tf_o / pk, 4),
-                                  "note": "fp32 includes the Wo^T pre-pass" if dt == torch.float32 else ""}}
-        del x, Wq, bq, Wo, bo, y, ws, o, wo_ws, gam, bet
+                                  "note": "fp32 includes the Wo^T pre-pass" if dt == torch.float32 else ""},
+                     "prepared_weights": {
+                         "sublayer_ms": round(ms_lp, 4), "sublayer_tflops": round(fl_l / (ms_lp * 1e-3) / 1e12, 2),
+                         "with_out_proj_ms": round(ms_op, 4),
+                         "with_out_proj_tflops": round(fl / (ms_op * 1e-3) / 1e12, 2),
+                         "prenorm_block_ms": round(ms_lnp, 4),
+                         "note": "la_layer_attn_prepared on weights prepared once (fp32: transposed) by "
+                                 "la_prepare_weight"}}
+        del x, Wq, bq, Wo, bo, y, ws, o, wo_ws, gam, bet, Wqp, Wop
 
     def small_latency(key, name):
         """Small-shape latency: back-to-back calls, host wall clock per call
@@ -535,7 +661,8 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
     qs = [q[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
     ks = [k[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
     vs = [v[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
-    del q, k, v
+    if not cpu_ok:
+        del q, k, v
     cache = api.KVCache(B, H, S, D, torch.bfloat16, device=dev)
     outs = [torch.empty_like(t) for t in qs]
     n = api.workspace_size(api.LA_OP_ATTN_CHUNKED, B, H, C, S, D, torch.bfloat16)
@@ -551,10 +678,33 @@ def other_workloads(args, dev, stream, flush, barrier, peaks):
     ms = _time_steps(chunked_step, kc, 1, flush, stream, barrier) / kc
     fl = flops.attn_flops(B, H, S, S, D, True)
     tf = fl / (ms * 1e-3) / 1e12
-    res["chunked bf16 causal B2 H16 S100000 D64, windows of 4096"] = {
-        "ms": round(ms, 3), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / _tensor_peak(torch.bfloat16, peaks), 4),
-        "gflop": round(fl / 1e9, 1), "windows": len(wins), "workspace_bytes": n,
-        "peak_device_bytes": torch.cuda.max_memory_allocated(dev)}
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    kt = kernel_times(api, chunked_step, 1, flush, stream)
+    r = {"ms": round(ms, 3), "tflops": round(tf, 2), "frac_of_tensor_peak": round(tf / _tensor_peak(torch.bfloat16, peaks), 4),
+         "gflop": round(fl / 1e9, 1), "windows": len(wins), "workspace_bytes": n, "peak_device_bytes": peak_mem,
+         "per_kernel_ms": {n_: round(t["ms"], 4) for n_, t in kt.items()}}
+    ka = kt.get("attn_fwd_kernel", {}).get("ms")
+    if ka:
+        r["attn_kernel"] = {"ms": round(ka, 4), "tflops": round(fl / (ka * 1e-3) / 1e12, 2),
+                            "frac_of_tensor_peak": round(fl / (ka * 1e-3) / 1e12 / _tensor_peak(torch.bfloat16, peaks), 4)}
+    if cpu_ok:
+        # the window-by-window result is attention over the whole sequence:
+        # the oracle on 256 sampled rows (window boundaries and the last row
+        # included), extrapolated per (query, key) pair
+        rows = inputs.sample_rows(B, H, S, n=256, seed=1234, forced=(0, 4095, 4096, 98303, 98304, 99999))
+        t0 = time.perf_counter()
+        import oracle
+        oracle.attn_rows(q, k, v, rows, causal=True)
+        t = time.perf_counter() - t0
+        pairs = _visible_keys(rows, S, S, True, None)
+        t_full = t / pairs * (fl / (4 * D))
+        r["cpu_baseline"] = {"value": round(fl / t_full / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "extrapolated": True,
+                             "sample": f"256 seeded sampled rows incl. window boundaries ({t:.2f} s, {pairs} query-key "
+                                       f"pairs, fp64, OpenMP); extrapolated per pair to the whole workload "
+                                       f"({t_full / 3600:.1f} h)"}
+        del q, k, v
+    res["chunked bf16 causal B2 H16 S100000 D64, windows of 4096"] = r
     st = api.get_last_error(stream)
     if st != api.LA_OK:
         raise RuntimeError(f"device status after the extra workloads: {api.status_string(st)}")
@@ -579,9 +729,71 @@ def cpu_baseline_sample(x_h, W_h, b_h, H, seconds=20.0):
         t_total += time.perf_counter() - t0
         done_b += 1
     fl = done_b * (flops.proj_flops(1, S, dm) + flops.attn_flops(1, H, S, S, D, False))
+    # the same on one core: the first batch entry with the oracle on one thread
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.layer_attn(x_h[:1].contiguous(), W_h, b_h, H)
+        t1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(0)
+    fl1 = flops.proj_flops(1, S, dm) + flops.attn_flops(1, H, S, S, D, False)
     return {"value": round(fl / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{done_b} of {x_h.shape[0]} batch entries of the sublayer workload ({t_total:.1f} s, fp64, OpenMP)"}
+            "sample": f"{done_b} of {x_h.shape[0]} batch entries of the sublayer workload ({t_total:.1f} s, fp64, OpenMP)",
+            "single_core": {"value": round(fl1 / t1 / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+                            "sample": f"1 batch entry of the sublayer workload ({t1:.1f} s, fp64, one thread)"}}
+
+
+def _visible_keys(rows, S_q, S_kv, causal, kv_len):
+    """Keys each sampled row (b, h, i) sees (the mask's definition, counted)."""
+    r = rows.numpy()
+    n = 0
+    for b, _, i in r:
+        lim = S_kv if kv_len is None else min(int(kv_len[b]), S_kv)
+        if causal:
+            lim = min(lim, int(i) + S_kv - S_q + 1)
+        n += max(lim, 0)
+    return n
+
+
+def cpu_attn_baseline(q, k, v, causal, kv_len, flops_total, full=False, seconds=2.0, seed=777):
+    """The fp64 oracle timed on the host cores on a bounded sample of an
+    attention workload.  full: the whole workload, repeated for about
+    `seconds`.  Otherwise seeded sampled rows (doubling their number until
+    the sample takes about `seconds`), timed, and extrapolated to the whole
+    workload per (query, visible key) pair."""
+    import oracle
+    from layer_attn_fwd_gb300 import inputs
+
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    cores = oracle.num_threads()
+    if full:
+        n, t = 0, 0.0
+        while n < 3 or t < seconds:
+            t0 = time.perf_counter()
+            oracle.attn(q, k, v, causal=causal, kv_len=kv_len)
+            t += time.perf_counter() - t0
+            n += 1
+        return {"value": round(flops_total * n / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": f"the whole workload, {n} runs ({t:.1f} s, fp64, OpenMP)", "extrapolated": False}
+    n_rows, t, pairs = 64, 0.0, 0
+    while True:
+        rows = inputs.sample_rows(B, H, S_q, n=n_rows, seed=seed)
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, rows, causal=causal, kv_len=kv_len)
+        t = time.perf_counter() - t0
+        pairs = _visible_keys(rows, S_q, S_kv, causal, kv_len)
+        if t >= seconds / 2 or n_rows >= 1 << 16:
+            break
+        n_rows *= 2
+    total_pairs = flops_total / (4 * D)
+    t_full = t / max(pairs, 1) * total_pairs
+    return {"value": round(flops_total / t_full / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_rows} seeded sampled rows ({t:.2f} s, {pairs} query-key pairs, fp64, OpenMP); "
+                      f"extrapolated per pair to the whole workload ({t_full:.1f} s)",
+            "extrapolated": True}
 
 
 def run_reference(args):
@@ -637,6 +849,18 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # no launcher set up the ranks: start one process per GPU the same way
+        # torchrun would (independent replicas; rank 0 prints the line)
+        if args.impl == "ours" and torch.cuda.device_count() < args.gpus:
+            ap.error(f"--gpus {args.gpus}: only {torch.cuda.device_count()} GPU(s) visible")
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.run(cmd).returncode)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -105,7 +105,10 @@ typedef struct {
  * ws, ws_bytes: workspace of la_workspace_size(LA_OP_QKV_PROJ, B, H, S, S,
  *   D, dt) bytes; fp32 needs 3*d_model*d_model*4 bytes there (the TF32
  *   tensor cores take K-major operands only, so the weight is transposed
- *   into it first), bf16/fp16 need none (ws may be NULL).
+ *   into it first), bf16/fp16 need none (ws may be NULL).  The workspace
+ *   argument is an addition to the projection's statement as a product
+ *   x.Wqkv + b: every scratch buffer of this library comes from the caller,
+ *   and the fp32 transpose needs one.
  * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE or
  * LA_ERR_CUDA.
  */
@@ -121,13 +124,20 @@ la_status la_qkv_proj(const void *x, const void *Wqkv, const void *bqkv,
  *   q [B, H, S_q, D]; k, v [B, H, S_kv, D]; o [B, H, S_q, D] output.
  *   causal, scale, kv_len: see the conventions above.
  *   ws, ws_bytes: workspace.  With at least
- *     la_workspace_size(LA_OP_ATTN_FWD, ...) bytes the call may split long
- *     key ranges across thread blocks and merge the partial results
- *     (split-KV); with less it runs unsplit.  Results agree to rounding
- *     either way.  bf16/fp16 need no workspace (ws may be NULL).  fp32 needs
- *     at least B*H*D*round_up(S_kv, 4)*4 bytes (rounded up to 256): V is
- *     transposed there first, because the TF32 tensor cores take K-major
- *     operands only; with less the call returns LA_ERR_WORKSPACE.
+ *     la_workspace_size(LA_OP_ATTN_FWD, ...) bytes the call schedules its
+ *     work items dynamically (one thread block per SM drawing items by
+ *     ticket; the ticket words live in ws) and may split long key ranges
+ *     across thread blocks and merge the partial results (split-KV).  With
+ *     less it gives every work item a thread block of its own and splits
+ *     only as far as ws allows.  Results agree to rounding either way.
+ *     bf16/fp16 need no workspace (ws may be NULL, slower on large shapes).
+ *     fp32 needs at least B*H*D*round_up(S_kv, 4)*4 bytes (rounded up to
+ *     256): V is transposed there first, because the TF32 tensor cores take
+ *     K-major operands only; with less the call returns LA_ERR_WORKSPACE.
+ *     ws needs no clearing.  Calls whose kernels may run at the same time
+ *     (on different streams, or a graph replay beside a direct call) must
+ *     use disjoint workspaces; a call may reuse its workspace as soon as the
+ *     previous call on it is ordered before it (same stream).
  * S_q == 0 is a no-op; S_kv == 0 writes zero rows.  q and o may be NULL
  * only when S_q == 0, k and v only when S_kv == 0.
  * Returns LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE or
@@ -233,10 +243,14 @@ la_status la_layernorm(const void *x, const void *gamma, const void *beta, void 
                        int M, int d, float eps, la_dtype dt, la_stream_t st);
 
 /*
- * The pre-norm attention block: la_layernorm(x), then the sublayer of
- * la_layer_attn on the normalised activations (stored in the element type
- * dt in between), then, when Wo is not NULL, the output projection of
- * la_out_proj:
+ * The pre-norm attention block: LayerNorm of x as la_layernorm computes it,
+ * fused into the Q/K/V projection ("Shape-Aware Attention", section What's
+ * next: fusing LayerNorm), then the attention of la_layer_attn and, when Wo
+ * is not NULL, the output projection of la_out_proj.  A pre-pass computes
+ * each row's statistics (mean and 1/sqrt(var + eps), fp32, 8 bytes a row);
+ * the projection normalises every x tile in shared memory as it loads it and
+ * rounds it to the operand type of its products (dt; TF32 for fp32), so the
+ * normalised activations are never written to memory:
  *   y [B, S, d_model] = [merge_heads(attention(LN(x) . Wqkv + bqkv)) . Wo + bo]
  * gamma, beta [d_model] and eps as for la_layernorm; Wo [d_model, d_model]
  * and bo [d_model] may be NULL (bo must be NULL when Wo is).  Arguments
@@ -254,6 +268,34 @@ la_status la_layer_attn_ln(const void *x, const void *gamma, const void *beta, f
                            void *ws, size_t ws_bytes, la_stream_t st);
 
 /*
+ * Weights prepared once, as a server does when it loads a model: the layout
+ * the projection kernels read, so that la_layer_attn_prepared does no
+ * per-call conversion of its constant weights.  W [rows, cols] row-major
+ * (Wqkv: rows = d_model, cols = 3*d_model; Wo: rows = cols = d_model);
+ * Wp: a caller-owned buffer of rows*cols elements of the same type, not
+ * overlapping W.  fp32 writes the transpose W^T [cols, rows] (the TF32
+ * tensor cores take K-major operands only); bf16/fp16 copy W unchanged.
+ * rows and cols must be multiples of 64.  Asynchronous on st.  Returns LA_OK,
+ * LA_ERR_INVALID, LA_ERR_UNSUPPORTED or LA_ERR_CUDA.  The pages have no
+ * counterpart (their weights live in a framework's modules).
+ */
+la_status la_prepare_weight(const void *W, void *Wp, int rows, int cols, la_dtype dt, la_stream_t st);
+
+/*
+ * The block of la_layer_attn_ln on prepared weights: Wqkv_p and Wo_p are
+ * la_prepare_weight's outputs for Wqkv and Wo.  gamma and beta may both be
+ * NULL (no LayerNorm: the sublayer of la_layer_attn, or with Wo_p that of
+ * la_layer_attn_out); Wo_p and bo may be NULL (no output projection; bo
+ * must be NULL when Wo_p is).  ws: as for la_layer_attn_ln (its size covers
+ * every form).  Results equal those of the unprepared calls bit for bit.
+ */
+la_status la_layer_attn_prepared(const void *x, const void *gamma, const void *beta, float eps,
+                                 const void *Wqkv_p, const void *bqkv, const void *Wo_p, const void *bo, void *y,
+                                 int B, int S, int d_model, int H, int causal,
+                                 const int32_t *kv_len, la_dtype dt,
+                                 void *ws, size_t ws_bytes, la_stream_t st);
+
+/*
  * la_attn_fwd without a workspace, for callers that cannot allocate device
  * memory: a host framework whose plugin interface hands over only the input
  * and output tensors, a service that sizes all of its device memory once at
@@ -262,10 +304,11 @@ la_status la_layer_attn_ln(const void *x, const void *gamma, const void *beta, f
  * pages have no counterpart; it is an addition of this library.
  *
  * Same arguments, meaning and result as la_attn_fwd, minus ws/ws_bytes.  Its
- * scratch (split-KV partials; for fp32 also V transposed) is one static
- * device array of 16 MiB inside the library, which every GPU that loads the
- * library keeps until the process exits; the call itself allocates nothing
- * (no cudaMalloc, cudaFree or allocating library routine).
+ * scratch (the work-item ticket words, split-KV partials; for fp32 also V
+ * transposed) is one static device array of 16 MiB inside the library,
+ * which every GPU that loads the library keeps until the process exits; the
+ * call itself allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
  *   - Limit: fp32 needs B*H*D*round_up(S_kv, 4)*4 bytes of it (rounded up to
  *     256); a call beyond 16 MiB returns LA_ERR_WORKSPACE and launches
  *     nothing.  Split partials take what is left; a call that would want more
@@ -346,6 +389,25 @@ int la_is_checked_build(void);
  * LA_ERR_INVALID for another mode.
  */
 la_status la_debug_shrink_output_extent(int mode);
+
+/*
+ * Per-launch device timing, for measurement (the pages time their kernels
+ * with CUDA events on the stream; "Shape-Aware Attention", How we built it).
+ * la_profile_start(n): the next launches of this process (at most n, from
+ * any entry point) are each bracketed by two CUDA events recorded on the
+ * stream the kernel is launched on.  While recording is on, kernels are
+ * launched without programmatic dependent launch and an event sits between
+ * consecutive kernels of a call, so each kernel's time is its own (the
+ * overlap of a kernel's set-up with the previous kernel is lost).  The events are
+ * created on the host as launches are recorded (no device memory); do not
+ * record during stream capture.
+ * la_profile_stop(names, ms, max): turns recording off, waits for the
+ * recorded events, writes up to max (kernel name, milliseconds) pairs in
+ * launch order (names point to static strings) and returns how many were
+ * written, or -1 if a CUDA call failed.  Returns LA_ERR_INVALID for n < 1.
+ */
+la_status la_profile_start(int max_launches);
+int la_profile_stop(const char **names, float *ms, int max);
 
 /* Static, human-readable name of a status. */
 const char *la_status_string(la_status s);

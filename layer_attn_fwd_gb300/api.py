@@ -76,6 +76,14 @@ def load(path: str | None = None, reload: bool = False):
         lib.la_debug_shrink_output_extent.restype = I
         lib.la_is_checked_build.argtypes = []
         lib.la_is_checked_build.restype = I
+        lib.la_prepare_weight.argtypes = [P, P, I, I, I, P]
+        lib.la_prepare_weight.restype = I
+        lib.la_layer_attn_prepared.argtypes = [P, P, P, F, P, P, P, P, P, I, I, I, I, I, P, I, P, Z, P]
+        lib.la_layer_attn_prepared.restype = I
+        lib.la_profile_start.argtypes = [I]
+        lib.la_profile_start.restype = I
+        lib.la_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), I]
+        lib.la_profile_stop.restype = I
         lib.la_status_string.argtypes = [I]
         lib.la_status_string.restype = ctypes.c_char_p
         for name in ("la_qkv_proj", "la_attn_fwd", "la_attn_chunked", "la_layer_attn", "la_out_proj",
@@ -381,6 +389,53 @@ def layer_attn_ln(x, gamma, beta, Wqkv, bqkv, Wo, bo, H, causal=False, kv_len=No
     return y
 
 
+def prepare_weight(W, out=None, stream=None):
+    """A projection weight W [rows, cols] in the layout the projection
+    kernels read (fp32: W^T [cols, rows]; bf16/fp16: a copy), prepared once
+    for layer_attn_prepared."""
+    _spec(W, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be [rows, cols]")
+    _need(W, "W")
+    rows, cols = W.shape
+    shape = (cols, rows) if W.dtype == torch.float32 else (rows, cols)
+    _spec_opt(out, "out", shape, W.dtype)
+    Wp = torch.empty(shape, dtype=W.dtype, device=W.device) if out is None else out
+    _check(load().la_prepare_weight(_ptr(W), _ptr(Wp), rows, cols, _dt(W), _stream(stream)), "la_prepare_weight")
+    return Wp
+
+
+def layer_attn_prepared(x, Wqkv_p, bqkv, H, gamma=None, beta=None, Wo_p=None, bo=None, causal=False, kv_len=None,
+                        eps=1e-5, out=None, workspace=None, stream=None):
+    """The block of layer_attn_ln on prepared weights (prepare_weight): with
+    or without the LayerNorm (gamma, beta) and the output projection (Wo_p,
+    bo).  x [B,S,d] -> [B,S,d]."""
+    _spec(x, "x")
+    if x.dim() != 3:
+        raise ValueError("x must be [B, S, d_model]")
+    B, S, dm = x.shape
+    D = dm // H if H > 0 else 0
+    wshape = (3 * dm, dm) if x.dtype == torch.float32 else (dm, 3 * dm)
+    _spec(Wqkv_p, "Wqkv_p", wshape, x.dtype)
+    _spec_opt(bqkv, "bqkv", (3 * dm,), x.dtype)
+    _spec_opt(gamma, "gamma", (dm,), x.dtype)
+    _spec_opt(beta, "beta", (dm,), x.dtype)
+    _spec_opt(Wo_p, "Wo_p", (dm, dm), x.dtype)
+    _spec_opt(bo, "bo", (dm,), x.dtype)
+    _kvlen_spec(kv_len, B)
+    _spec_opt(out, "out", (B, S, dm), x.dtype)
+    _need(x, "x")
+    y = torch.empty_like(x) if out is None else out
+    if workspace is None:
+        workspace = _workspace(workspace_size(LA_OP_LAYER_ATTN_LN, B, H, S, S, D, x.dtype), x.device, None)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().la_layer_attn_prepared(_ptr(x), _ptr(gamma), _ptr(beta), float(eps), _ptr(Wqkv_p), _ptr(bqkv),
+                                         _ptr(Wo_p), _ptr(bo), _ptr(y), B, S, dm, H, int(bool(causal)),
+                                         _ptr(kv_len), _dt(x), _ptr(workspace), nbytes, _stream(stream)),
+           "la_layer_attn_prepared")
+    return y
+
+
 class Graph:
     """Library calls captured once and replayed as one CUDA graph.
 
@@ -406,6 +461,40 @@ class Graph:
 
     def replay(self):
         self.graph.replay()
+
+
+class Profile:
+    """Per-launch device times of the library's kernels (CUDA events on each
+    launch's stream; see la_profile_start in layerattn.h):
+
+        with api.Profile() as p:
+            ...library calls...
+        p.records  # [(kernel name, ms), ...] in launch order
+    """
+
+    def __init__(self, max_launches=4096):
+        self.max = int(max_launches)
+        self.records = []
+
+    def __enter__(self):
+        _check(load().la_profile_start(self.max), "la_profile_start")
+        return self
+
+    def __exit__(self, *exc):
+        names = (ctypes.c_char_p * self.max)()
+        ms = (ctypes.c_float * self.max)()
+        n = load().la_profile_stop(names, ms, self.max)
+        if n < 0:
+            raise RuntimeError("la_profile_stop: a CUDA call failed")
+        self.records = [(names[i].decode(), float(ms[i])) for i in range(n)]
+        return False
+
+    def by_kernel(self):
+        """{kernel name: [ms of each launch]}."""
+        out = {}
+        for name, ms in self.records:
+            out.setdefault(name, []).append(ms)
+        return out
 
 
 def last_error_detail() -> int:

@@ -12,6 +12,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "la_device.cuh"
 #include "la_internal.h"
@@ -116,7 +117,7 @@ la_status map_bhsd(CUtensorMap* m, const void* base, la_dtype dt, int B, int H, 
 
 // 2-D map over a row-major [rows, cols] matrix.
 la_status map_2d(CUtensorMap* m, const void* base, la_dtype dt, long long rows, long long cols, int box_rows,
-                 int box_cols) {
+                 int box_cols, bool raw = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return LA_ERR_CUDA;
   const long long e = elem_bytes(dt);
@@ -124,7 +125,7 @@ la_status map_2d(CUtensorMap* m, const void* base, la_dtype dt, long long rows, 
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * e)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, tma_type(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(m, raw && dt == LA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tma_type(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LA_OK : LA_ERR_CUDA;
@@ -140,6 +141,18 @@ struct Plan {
   int tiles_per_split = 1;
   size_t ws_bytes = 0;  // partials the plan needs
 };
+
+// The persistent attention's ticket word and done word (two 64-bit words,
+// padded so that what follows stays 256-byte aligned).
+constexpr size_t kSchedBytes = 256;
+
+// Tag of the next persistent launch (never 0, the value of a word at rest).
+unsigned next_sched_tag() {
+  static std::atomic<unsigned> tag{0};
+  unsigned t = tag.fetch_add(1u) + 1u;
+  while (t == 0u) t = tag.fetch_add(1u) + 1u;
+  return t;
+}
 
 size_t split_bytes(int splits, int B, int H, int S_q, int D) {
   if (splits <= 1) return 0;
@@ -219,13 +232,22 @@ struct KVView {
 };
 
 // Attention: q [B,H,S_q,D] contiguous; o with the given element strides.
-// Scratch from ws: the fp32 V^T (unless given), then the split partials.
+// Scratch from ws, in this order: the fp32 V^T (unless given; required),
+// the ticket words of the persistent form (without room for them every item
+// gets a CTA of its own), then the split partials (the plan splits only as
+// far as what is left allows).
 la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb, long long o_sh, long long o_ss,
                         int B, int H, int S_q, int S_kv, int D, int causal, float scale, const int32_t* kv_len,
                         la_dtype dt, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (S_q == 0) return LA_OK;
   AttnShape sh;
   if (!attn_shape(dt, D, &sh)) return LA_ERR_UNSUPPORTED;
+  // No key at all: every row is a zero row.  Both output layouts used here
+  // (head-major, and heads merged) cover exactly B*H*S_q*D contiguous
+  // elements; no tensor map is built (a V^T map over zero keys has no valid
+  // stride).
+  if (S_kv == 0)
+    return cuda_status(cudaMemsetAsync(o, 0, static_cast<size_t>(B) * H * S_q * D * elem_bytes(dt), st));
   uint8_t* w = static_cast<uint8_t*>(ws);
   size_t w_left = ws == nullptr ? 0 : ws_bytes;
   const void* vt = kv.vt;
@@ -240,6 +262,12 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
     vt = w;
     w += need;
     w_left -= need;
+  }
+  unsigned long long* sched = nullptr;
+  if (w_left >= kSchedBytes) {
+    sched = reinterpret_cast<unsigned long long*>(w);
+    w += kSchedBytes;
+    w_left -= kSchedBytes;
   }
   const Plan p = make_plan(dt, B, H, S_q, S_kv, D, w_left, device_sms());
   uint32_t* err = error_word();
@@ -278,6 +306,8 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
   a.num_qblk = p.num_qblk;
   a.tiles_per_split = p.tiles_per_split;
   a.err = err;
+  a.sched = sched;
+  a.sched_gen = next_sched_tag();
   a.skip_loads = g_skip_loads_once.exchange(0);
 #if LA_CHECKED
   // extents for the bounds checks: [B, H, S_q, D] elements either layout
@@ -322,7 +352,7 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
 size_t attn_ws_bytes(la_dtype dt, int B, int H, int S_q, int S_kv, int D, bool need_vt) {
   if (S_q == 0) return 0;
   const size_t vt = need_vt ? vt_bytes(dt, B, H, S_kv, D) : 0;
-  return vt + make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), device_sms()).ws_bytes;
+  return vt + kSchedBytes + make_plan(dt, B, H, S_q, S_kv, D, static_cast<size_t>(-1), device_sms()).ws_bytes;
 }
 
 la_status check_proj_args(const void* x, const void* W, const void* bias, const void* q, const void* k,
@@ -339,12 +369,21 @@ la_status check_proj_args(const void* x, const void* W, const void* bias, const 
   return LA_OK;
 }
 
-// Projection; scratch from ws: the fp32 Wqkv^T (transposed there first,
-// unless wt_ready says it already is).  With vt != nullptr (fp32 sublayer) V
-// is written as V^T [B, H, D, vt_ld] there instead of into v.
+// LayerNorm in front of the projection: per-row statistics (from the stats
+// pre-pass) and gamma, beta; the projection normalises x as it loads it.
+struct LnIn {
+  const float2* stats = nullptr;
+  const void* gamma = nullptr;
+  const void* beta = nullptr;
+};
+
+// Projection.  w_kernel: the weight already in the layout the kernel reads
+// (fp32: Wqkv^T [3d, d]; half precision: Wqkv itself), or null: then fp32
+// transposes W into ws first.  With vt != nullptr (fp32 sublayer) V is
+// written as V^T [B, H, D, vt_ld] there instead of into v.
 la_status run_proj(const void* x, const void* W, const void* bias, void* q, void* k, void* v, int B, int S,
-                   int d_model, int H, float q_scale, la_dtype dt, void* ws, size_t ws_bytes, bool wt_ready,
-                   void* vt, long long vt_ld, cudaStream_t st) {
+                   int d_model, int H, float q_scale, la_dtype dt, void* ws, size_t ws_bytes, const void* w_kernel,
+                   void* vt, long long vt_ld, cudaStream_t st, const LnIn& ln = LnIn()) {
   const long long M = static_cast<long long>(B) * S;
   if (M == 0) return LA_OK;
   ProjShape ps;
@@ -352,16 +391,20 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   uint32_t* err = error_word();
   if (err == nullptr) return LA_ERR_CUDA;
   CUtensorMap tx, tw;
-  la_status s = map_2d(&tx, x, dt, M, d_model, kTileM, ps.box_cols);
+  // with LayerNorm in front, fp32 x is copied unrounded (it is normalised,
+  // then rounded to TF32, in shared memory)
+  la_status s = map_2d(&tx, x, dt, M, d_model, kTileM, ps.box_cols, ln.stats != nullptr);
   if (s != LA_OK) return s;
   if (ps.w_transposed) {
-    const size_t need = wt_bytes(dt, d_model);
-    if (ws == nullptr || ws_bytes < need) return LA_ERR_WORKSPACE;
-    if (!wt_ready && launch_transpose32(W, 0, ws, d_model, 1, d_model, 3 * d_model, st) != cudaSuccess)
-      return LA_ERR_CUDA;
-    s = map_2d(&tw, ws, dt, 3LL * d_model, d_model, ps.block_n, ps.box_cols);
+    if (w_kernel == nullptr) {
+      const size_t need = wt_bytes(dt, d_model);
+      if (ws == nullptr || ws_bytes < need) return LA_ERR_WORKSPACE;
+      if (launch_transpose32(W, 0, ws, d_model, 1, d_model, 3 * d_model, st) != cudaSuccess) return LA_ERR_CUDA;
+      w_kernel = ws;
+    }
+    s = map_2d(&tw, w_kernel, dt, 3LL * d_model, d_model, ps.block_n, ps.box_cols);
   } else {
-    s = map_2d(&tw, W, dt, d_model, 3LL * d_model, ps.box_k_rows, ps.box_cols);
+    s = map_2d(&tw, w_kernel != nullptr ? w_kernel : W, dt, d_model, 3LL * d_model, ps.box_k_rows, ps.box_cols);
   }
   if (s != LA_OK) return s;
   ProjArgs a;
@@ -380,6 +423,9 @@ la_status run_proj(const void* x, const void* W, const void* bias, void* q, void
   a.err = err;
   a.v_transposed = vt != nullptr;
   a.S_pad = vt_ld;
+  a.ln_stats = ln.stats;
+  a.ln_gamma = ln.gamma;
+  a.ln_beta = ln.beta;
 #if LA_CHECKED
   a.qk_elems = M * d_model;
   a.v_elems = vt != nullptr ? static_cast<long long>(B) * d_model * vt_ld : M * d_model;
@@ -446,11 +492,11 @@ size_t layer_fixed_bytes(int B, int S, int d_model, int H, la_dtype dt) {
 }
 
 // The sublayer without its output projection: ws holds q | k | v (fp32: V^T
-// [B,H,D,S_pad]) | fp32 Wqkv^T | split partials.  With wt_ready the fp32
-// Wqkv^T is already in place.
+// [B,H,D,S_pad]) | fp32 Wqkv^T | split partials.  w_kernel: the weight in
+// the projection kernel's layout (see run_proj), or null.
 la_status run_layer(const void* x, const void* Wqkv, const void* bqkv, void* o, int B, int S, int d_model, int H,
-                    int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes, bool wt_ready,
-                    cudaStream_t cs) {
+                    int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes, const void* w_kernel,
+                    cudaStream_t cs, const LnIn& ln = LnIn()) {
   const int D = d_model / H;
   const size_t one = layer_qkv_bytes(B, S, d_model, dt);
   const size_t vbytes = dt == LA_F32 ? vt_bytes(dt, B, H, S, D) : one;
@@ -461,8 +507,8 @@ la_status run_layer(const void* x, const void* Wqkv, const void* bqkv, void* o, 
   void *q = w, *k = w + one, *v = w + 2 * one;
   uint8_t* wt = w + 2 * one + vbytes;
   const bool vt = dt == LA_F32;
-  la_status s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, wt, wt_bytes(dt, d_model), wt_ready,
-                         vt ? v : nullptr, vt_pad(S), cs);
+  la_status s = run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, 1.f, dt, wt, wt_bytes(dt, d_model), w_kernel,
+                         vt ? v : nullptr, vt_pad(S), cs, ln);
   if (s != LA_OK) return s;
   const float scale = 1.0f / sqrtf(static_cast<float>(D));
   const KVView kv{k, v, S, vt ? v : nullptr, vt_pad(S)};
@@ -490,53 +536,111 @@ la_status check_ln_args(const void* gamma, const void* beta, float eps) {
   return LA_OK;
 }
 
-// Workspace of the block: the normalised x (with LayerNorm) | the merged
+// Row statistics of the LayerNorm in front: (mean, 1 / sqrt(var + eps)) per row.
+size_t ln_stats_bytes(int B, int S) { return round_up(static_cast<size_t>(B) * S * sizeof(float2), 256); }
+
+// Workspace of the block: the row statistics (with LayerNorm) | the merged
 // attention output and the fp32 Wo^T (with the output projection) | the
 // sublayer's own workspace.
 size_t block_fixed_bytes(int B, int S, int d_model, int H, la_dtype dt, bool ln, bool out) {
   const size_t act = layer_qkv_bytes(B, S, d_model, dt);
-  return (ln ? act : 0) + (out ? act + wot_bytes(dt, d_model) : 0) + layer_fixed_bytes(B, S, d_model, H, dt);
+  return (ln ? ln_stats_bytes(B, S) : 0) + (out ? act + wot_bytes(dt, d_model) : 0) +
+         layer_fixed_bytes(B, S, d_model, H, dt);
 }
 
 // The attention block: [LayerNorm] -> projection -> attention (heads merged)
 // -> [output projection].  Arguments already validated.  For fp32 the
 // weight transposes come first: Wqkv^T as an ordinary launch (everything
-// before this call has finished), then Wo^T and the LayerNorm, which may
-// overlap it (each waits for the grid before it before exiting).
+// before this call has finished), then Wo^T and the LayerNorm statistics,
+// which may overlap it (each waits for the grid before it before exiting).
+// prepared: Wqkv and Wo are already in the kernels' layout
+// (la_prepare_weight), so nothing is transposed.
 la_status run_block(const void* x, const void* gamma, const void* beta, float eps, const void* Wqkv,
                     const void* bqkv, const void* Wo, const void* bo, void* y, int B, int S, int d_model, int H,
-                    int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes, cudaStream_t cs) {
+                    int causal, const int32_t* kv_len, la_dtype dt, void* ws, size_t ws_bytes, cudaStream_t cs,
+                    bool prepared = false) {
   const bool ln = gamma != nullptr, out = Wo != nullptr;
   if (ws_bytes < block_fixed_bytes(B, S, d_model, H, dt, ln, out)) return LA_ERR_WORKSPACE;
   if (S == 0) return LA_OK;
   const size_t act = layer_qkv_bytes(B, S, d_model, dt);
   const long long M = static_cast<long long>(B) * S;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void* xn = ln ? w : nullptr;
-  w += ln ? act : 0;
+  float2* stats = ln ? reinterpret_cast<float2*>(w) : nullptr;
+  w += ln ? ln_stats_bytes(B, S) : 0;
   void* o = out ? w : y;
   void* wot = out ? w + act : nullptr;
   w += out ? act + wot_bytes(dt, d_model) : 0;
   const size_t lw_bytes = ws_bytes - static_cast<size_t>(w - static_cast<uint8_t*>(ws));
   bool first = true;  // the first launch of the call is an ordinary one
-  if (dt == LA_F32) {
+  const void* w_kernel = prepared ? Wqkv : nullptr;
+  if (prepared) {
+    wot = const_cast<void*>(Wo);
+  } else if (dt == LA_F32) {
     uint8_t* wt = w + 2 * act + vt_bytes(dt, B, H, S, d_model / H);  // where run_layer keeps Wqkv^T
     if (launch_transpose32(Wqkv, 0, wt, d_model, 1, d_model, 3 * d_model, cs) != cudaSuccess) return LA_ERR_CUDA;
     first = false;
+    w_kernel = wt;
     if (out && launch_transpose32(Wo, 0, wot, d_model, 1, d_model, d_model, cs, true) != cudaSuccess)
       return LA_ERR_CUDA;
   }
-  if (ln) {
-    if (launch_layernorm(dt, x, gamma, beta, xn, M, d_model, eps, cs, !first) != cudaSuccess) return LA_ERR_CUDA;
+  LnIn lni;
+  if (ln) {  // the statistics only; the projection normalises x as it loads it
+    if (launch_layernorm(dt, x, gamma, beta, nullptr, M, d_model, eps, cs, !first, stats) != cudaSuccess)
+      return LA_ERR_CUDA;
     first = false;
+    lni.stats = stats;
+    lni.gamma = gamma;
+    lni.beta = beta;
   }
-  la_status s = run_layer(ln ? xn : x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, w, lw_bytes,
-                          dt == LA_F32, cs);
+  la_status s = run_layer(x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, w, lw_bytes, w_kernel, cs, lni);
   if (s != LA_OK || !out) return s;
   return run_out_proj(o, Wo, wot, bo, y, M, d_model, dt, cs);
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// per-launch timing (la_profile_start / la_profile_stop)
+// ---------------------------------------------------------------------------
+namespace {
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_prof;
+size_t g_prof_max = 0;
+std::atomic<bool> g_prof_on{false};
+// index of the record the launch being made on this thread opened, or -1
+// (past the record limit, nothing is recorded for it)
+thread_local long t_prof_open = -1;
+}  // namespace
+
+bool prof_on() { return g_prof_on.load(std::memory_order_relaxed); }
+
+void prof_before(cudaStream_t st, const char* name) {
+  t_prof_open = -1;
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof.size() >= g_prof_max) return;
+  ProfRecord r{name, nullptr, nullptr};
+  if (cudaEventCreate(&r.start) != cudaSuccess) return;
+  if (cudaEventCreate(&r.stop) != cudaSuccess) {
+    cudaEventDestroy(r.start);
+    return;
+  }
+  cudaEventRecord(r.start, st);
+  t_prof_open = static_cast<long>(g_prof.size());
+  g_prof.push_back(r);
+}
+
+void prof_after(cudaStream_t st) {
+  if (t_prof_open < 0) return;  // this launch was not recorded
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (static_cast<size_t>(t_prof_open) < g_prof.size()) cudaEventRecord(g_prof[t_prof_open].stop, st);
+  t_prof_open = -1;
+}
+
 }  // namespace la
 
 using namespace la;
@@ -549,7 +653,7 @@ la_status la_qkv_proj(const void* x, const void* Wqkv, const void* bqkv, void* q
   if (s != LA_OK) return s;
   if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
   if (S > 0 && (ws == nullptr ? 0 : ws_bytes) < wt_bytes(dt, d_model)) return LA_ERR_WORKSPACE;
-  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, ws, ws_bytes, false, nullptr, 0,
+  return run_proj(x, Wqkv, bqkv, q, k, v, B, S, d_model, H, q_scale, dt, ws, ws_bytes, nullptr, nullptr, 0,
                   reinterpret_cast<cudaStream_t>(st));
 }
 
@@ -605,7 +709,7 @@ la_status la_layer_attn(const void* x, const void* Wqkv, const void* bqkv, void*
                         la_stream_t st) {
   la_status s = check_layer_args(x, Wqkv, bqkv, o, ws, B, S, d_model, H, kv_len, dt);
   if (s != LA_OK) return s;
-  return run_layer(x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, ws, ws_bytes, false,
+  return run_layer(x, Wqkv, bqkv, o, B, S, d_model, H, causal, kv_len, dt, ws, ws_bytes, nullptr,
                    reinterpret_cast<cudaStream_t>(st));
 }
 
@@ -661,6 +765,39 @@ la_status la_layer_attn_ln(const void* x, const void* gamma, const void* beta, f
   }
   return run_block(x, gamma, beta, eps, Wqkv, bqkv, Wo, bo, y, B, S, d_model, H, causal, kv_len, dt, ws, ws_bytes,
                    reinterpret_cast<cudaStream_t>(st));
+}
+
+la_status la_prepare_weight(const void* W, void* Wp, int rows, int cols, la_dtype dt, la_stream_t st) {
+  if (!W || !Wp || rows < 1 || cols < 1 || !dtype_ok(dt)) return LA_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(Wp)) return LA_ERR_INVALID;
+  if (rows % 64 != 0 || cols % 64 != 0) return LA_ERR_UNSUPPORTED;
+  const size_t bytes = static_cast<size_t>(rows) * cols * elem_bytes(dt);
+  const char* a = static_cast<const char*>(W);
+  const char* b = static_cast<const char*>(Wp);
+  if (a < b + bytes && b < a + bytes) return LA_ERR_INVALID;  // overlapping buffers
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
+  if (dt == LA_F32) return cuda_status(launch_transpose32(W, 0, Wp, rows, 1, rows, cols, cs));
+  return cuda_status(cudaMemcpyAsync(Wp, W, bytes, cudaMemcpyDeviceToDevice, cs));
+}
+
+la_status la_layer_attn_prepared(const void* x, const void* gamma, const void* beta, float eps, const void* Wqkv_p,
+                                 const void* bqkv, const void* Wo_p, const void* bo, void* y, int B, int S,
+                                 int d_model, int H, int causal, const int32_t* kv_len, la_dtype dt, void* ws,
+                                 size_t ws_bytes, la_stream_t st) {
+  la_status s = check_layer_args(x, Wqkv_p, bqkv, y, ws, B, S, d_model, H, kv_len, dt);
+  if (s != LA_OK) return s;
+  if (gamma != nullptr || beta != nullptr) {
+    s = check_ln_args(gamma, beta, eps);
+    if (s != LA_OK) return s;
+  }
+  if (Wo_p != nullptr) {
+    s = check_out_proj_args(ws, Wo_p, bo, y, static_cast<long long>(B) * S, d_model, dt);
+    if (s != LA_OK) return s;
+  } else if (bo != nullptr) {
+    return LA_ERR_INVALID;
+  }
+  return run_block(x, gamma, beta, eps, Wqkv_p, bqkv, Wo_p, bo, y, B, S, d_model, H, causal, kv_len, dt, ws,
+                   ws_bytes, reinterpret_cast<cudaStream_t>(st), true);
 }
 
 size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtype dt) {
@@ -729,6 +866,41 @@ la_status la_attn_fwd_noalloc(const void* q, const void* k, const void* v, void*
   return run_attention(q, kv, o, static_cast<long long>(H) * S_q * D, static_cast<long long>(S_q) * D, D, B, H,
                        S_q, S_kv, D, causal, scale, kv_len, dt, scratch, kNoAllocScratchBytes,
                        reinterpret_cast<cudaStream_t>(st));
+}
+
+la_status la_profile_start(int max_launches) {
+  if (max_launches < 1) return LA_ERR_INVALID;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (auto& r : g_prof) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof.clear();
+  g_prof.reserve(static_cast<size_t>(max_launches));
+  g_prof_max = static_cast<size_t>(max_launches);
+  g_prof_on.store(true);
+  return LA_OK;
+}
+
+int la_profile_stop(const char** names, float* ms, int max) {
+  g_prof_on.store(false);
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  int n = 0;
+  bool ok = true;
+  for (auto& r : g_prof) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      ok = false;
+    if (n < max && names != nullptr && ms != nullptr) {
+      names[n] = r.name;
+      ms[n] = t;
+    }
+    ++n;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof.clear();
+  return ok ? (n < max ? n : max) : -1;
 }
 
 la_status la_get_last_error(la_stream_t st) {

@@ -89,10 +89,9 @@ constexpr int pow2_at_least(int x) {
 // PERS: the persistent form, for launches with more work items than SMs;
 // otherwise each CTA runs exactly one item (no item hand-off, and the
 // epilogue stages its stores in the dead Q tiles).
-template <typename T, int D_, int NQ_, int BN_, int NS_, int EMU_, bool PERS = true>
+template <typename T, int D_, int NQ_, int BN_, int NS_, bool SP_, bool PERS = true>
 struct Cfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, NS = NS_;
-  static constexpr int EMU = EMU_;  // of every 8 score columns, how many use the FMA-pipe exp2
   static constexpr int E = sizeof(T);
   static constexpr int CW = 128 / E;            // elements per 128-byte swizzle row
   static constexpr int NCH = D / CW;            // 128-byte chunks per row of D elements
@@ -100,22 +99,33 @@ struct Cfg {
   static constexpr int KV_CHUNK = BN * 128;
   static constexpr int Q_TILE = NCH * Q_CHUNK;
   static constexpr int KV_TILE = NCH * KV_CHUNK;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
-  static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp (PERS)
-  static constexpr int OFF_BAR = OFF_STG + (PERS ? NQ * 4 * 4096 : 0);
-  // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ], o_full[NQ],
-  // o_free[NQ], mma_done, qt_full, item_full[NR], item_empty[NR]
-  static constexpr int NR = 4;  // work items handed from the scheduling thread to the other roles
-  static constexpr int NBAR = 2 + 4 * NS + 4 * NQ + 2 + 2 * NR;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, then the item ring
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 4 * NR + 1024;  // + slack for 1024-byte alignment
   // Q as the A operand of QK^T from tensor memory when it fits: the product
   // then reads only K from shared memory (half the operand traffic).
   static constexpr int QCOLS = D * E / 4;                  // 32-bit TMEM columns of one Q row
-  static constexpr bool QT = NQ * (BN + D + QCOLS) <= 512;
-  static constexpr int TILE_COLS = BN + D + (QT ? QCOLS : 0);  // per query tile: S|P, O, then Q
+  // SP: P gets tensor-memory columns of its own instead of overwriting S,
+  // so that QK^T of the next key tile runs while the softmax of this one
+  // works (chosen per configuration: it pays where the tile's MMAs, not its
+  // softmax, are the longer part).  Without Q in tensor memory Q stays in
+  // shared memory, double buffered so the next item's Q loads meanwhile.
+  static constexpr bool SP = SP_;
+  static constexpr int P_COLS = SP ? BN * E / 4 : 0;       // 32-bit TMEM columns of P (SP)
+  static constexpr bool QT = NQ * (BN + P_COLS + D + QCOLS) <= 512;
+  static constexpr int QB = (SP && !QT) ? 2 : 1;           // Q buffers in shared memory
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB * NQ * Q_TILE;
+  static constexpr int OFF_V = OFF_K + NS * KV_TILE;
+  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp (PERS)
+  static constexpr int OFF_BAR = OFF_STG + (PERS ? NQ * 4 * 4096 : 0);
+  // q_full[QB], q_empty[QB], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ],
+  // o_full[NQ], o_free[NQ], mma_done, qt_full, item_full[NR], item_empty[NR], s_free[NQ], pv_done[NQ]
+  static constexpr int NR = 4;  // work items handed from the scheduling thread to the other roles
+  static constexpr int NBAR = 2 * QB + 4 * NS + 4 * NQ + 2 + 2 * NR + 2 * NQ;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, then the item ring
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 4 * NR + 1024;  // + slack for 1024-byte alignment
+  // per query tile: S (P over it, or P after it with SP), O, then Q (QT)
+  static constexpr int P_COL = SP ? BN : 0;
+  static constexpr int O_COL = BN + P_COLS;
+  static constexpr int TILE_COLS = O_COL + D + (QT ? QCOLS : 0);
   static constexpr int TMEM_COLS = pow2_at_least(NQ * TILE_COLS);
   static constexpr int QK_STEPS = D * E / 32;              // one MMA consumes 32 bytes of a row
   static constexpr int PV_ROWS = 32 / E;                   // keys per PV MMA (16, or 8 for tf32)
@@ -129,11 +139,11 @@ struct Cfg {
   // (measured: fp32 D=64 +5%, bf16 D=64 +3%).  With Q in shared memory one
   // warp, which keeps the strict PV_0, S_0, PV_1, S_1 order (measured: two
   // warps cost bf16 D=128 10%).
-  static constexpr int MW = QT ? NQ : 1;
+  static constexpr int MW = (QT || SP) ? NQ : 1;
   // One barrier pair per key/value stage (KVM) where measured faster: with Q
   // in tensor memory (fp32 D=64 +3%, bf16 D=64 +7%); bf16 D=128 with its
   // two 64 KB stages needs the key slot back before PV is done (-7%).
-  static constexpr bool KVM = QT;
+  static constexpr bool KVM = QT || SP;
   static constexpr int THREADS = NQ * 128 + 32 + 32 * MW;
   static constexpr int WARP_TMA = NQ * 4;
   static constexpr int WARP_MMA = NQ * 4 + 1;  // first MMA warp
@@ -153,31 +163,6 @@ __device__ __forceinline__ void load_row(uint32_t taddr, uint32_t (&s)[BN]) {
     tmem_ld_x128(taddr, s);
   } else {
     tmem_ld_x64(taddr, s);
-  }
-}
-
-// Store P (already exponentiated, in s[] as fp32 bits) over the S columns.
-template <typename T, int BN>
-__device__ __forceinline__ void store_p(uint32_t taddr, uint32_t (&s)[BN]) {
-  if constexpr (Elem<T>::tf32) {
-    // Round to TF32 (nearest, ties away): add half a TF32 ulp to the bit
-    // pattern; the kind::tf32 product reads only the top 19 bits of each
-    // 32-bit element, so the low 13 bits need no masking.  P >= 0 and
-    // finite here, so the carry into the exponent is the correct rounding.
-    // (A conversion instruction per element measured ~1000 cycles a row.)
-#pragma unroll
-    for (int c = 0; c < BN; ++c) s[c] = s[c] + 0x1000u;
-    tmem_st_x64_at<0>(taddr, s);
-    if constexpr (BN == 128) tmem_st_x64_at<64>(taddr + 64, s);
-  } else {
-    uint32_t pk[BN / 2];
-#pragma unroll
-    for (int c = 0; c < BN / 2; ++c) pk[c] = Elem<T>::pack2(u2f(s[2 * c]), u2f(s[2 * c + 1]));
-    if constexpr (BN == 128) {
-      tmem_st_x64(taddr, pk);
-    } else {
-      tmem_st_x32(taddr, pk);
-    }
   }
 }
 
@@ -281,29 +266,55 @@ __device__ __forceinline__ int sel(const int (&je)[NQ], int t) {
   return v;
 }
 
+// The ticket word and the done word each hold a launch tag in their high half
+// and a count in their low half.  claim(): once per CTA, before its first
+// increment of the word; a word not yet carrying this launch's tag (zero
+// after a reset, or whatever a fresh workspace held) is set to (tag, 0) by
+// one compare-and-swap.  If that swap fails, another CTA of the launch has
+// just claimed the word (nothing else writes it), so one attempt suffices and
+// no CTA ever loops on it; increments are then plain atomic adds.
+__device__ __forceinline__ void claim(unsigned long long* w, unsigned tag) {
+  const unsigned long long cur = atomicAdd(w, 0ull);  // read at the L2, not from a stale line
+  if (static_cast<unsigned>(cur >> 32) != tag) atomicCAS(w, cur, static_cast<unsigned long long>(tag) << 32);
+}
+// Increment of a claimed word: the count before it, or false (and the error
+// word latched) if the word does not carry this launch's tag.
+__device__ __forceinline__ bool tagged_add(unsigned long long* w, unsigned tag, uint32_t* err, unsigned* before) {
+  const unsigned long long old = atomicAdd(w, 1ull);
+  if (static_cast<unsigned>(old >> 32) != tag) {
+    atomicOr(err, DEVERR_INTERNAL);
+    return false;
+  }
+  *before = static_cast<unsigned>(old);
+  return true;
+}
+
 // Persistent: one CTA per SM.  CTA c starts with item c; further items come
-// from a global ticket counter (heaviest first, whichever CTA is free next),
-// ticket t meaning item gridDim.x + t.  Barrier phases and the key/value
-// ring continue from one item to the next, so an item's loads are issued
-// while the previous item finishes.  Tickets are counted from zero in
-// a.sched[0]; every CTA draws until it gets one past the last item, then
-// counts itself done in a.sched[1], and the last CTA done resets both, so
-// every launch (or CUDA-graph replay) finds them at zero.
-template <typename T, int D, int NQ, int BN, int NS, int EMU, bool PERS>
-__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
+// by ticket (heaviest first, whichever CTA is free next), ticket t meaning
+// item gridDim.x + t.  Barrier phases and the key/value ring continue from
+// one item to the next, so an item's loads are issued while the previous
+// item finishes.  The ticket word a.sched[0] and the done word a.sched[1]
+// live in the caller's workspace, so launches that run at the same time
+// (disjoint workspaces) never share them; both carry this launch's tag
+// (claim), so a fresh workspace needs no clearing.  Every CTA draws until it
+// gets a ticket past the last item, then counts itself done, and the last
+// CTA done sets both words to zero, so a replay of the launch from a CUDA
+// graph (same tag) claims them afresh and starts again from ticket 0.
+template <typename T, int D, int NQ, int BN, int NS, bool SP, bool PERS>
+__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using C = Cfg<T, D, NQ, BN, NS, EMU, PERS>;
+  using C = Cfg<T, D, NQ, BN, NS, SP, PERS>;
   constexpr bool TF32 = Elem<T>::tf32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = q_full + 1;  // Q in shared memory: the item's last QK^T is done (one MMA commit)
+  uint64_t* q_full = bars;          // [QB]
+  uint64_t* q_empty = q_full + C::QB;  // [QB] Q in shared memory: the item's MMAs are done (one commit per MMA warp)
   // With KVM the key and value tiles of a stage share k_full / k_empty (one
   // wait and one commit per key tile; v_full / v_empty unused); otherwise K
   // and V have their own, so that a key slot frees as soon as QK^T is done.
-  uint64_t* k_full = q_empty + 1;
+  uint64_t* k_full = q_empty + C::QB;
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
@@ -315,9 +326,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
   uint64_t* qt_full = mma_done + 1;  // Q copied into tensor memory (one arrive per softmax warp)
   uint64_t* item_full = qt_full + 1;  // ring slot holds the next item (-1: none left)
   uint64_t* item_empty = item_full + C::NR;  // every consumer warp has read the slot
-  // the Q shared tiles may take the next item's load once: the copy into
-  // tensor memory is done (QT), or the item's last QK^T has completed
-  uint64_t* q_free = C::QT ? qt_full : q_empty;
+  uint64_t* s_free = item_empty + C::NR;     // SP: S of tile t read into registers (one arrive per softmax warp)
+  uint64_t* pv_done = s_free + NQ;           // SP: the PV product of tile t completed (P and O free again)
+  // the Q shared tiles (buffer b) may take the next item's load once: the
+  // copy into tensor memory is done (QT), or the item's MMAs have completed
+  auto q_free = [&](int b) -> uint64_t* { return C::QT ? qt_full : &q_empty[b]; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
@@ -327,8 +340,10 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
 
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int b = 0; b < C::QB; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], C::MW);  // one commit per MMA warp
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], C::MW);  // one commit per MMA warp
@@ -340,6 +355,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
       mbar_init(&p_full[t], 4);  // one arrive per softmax warp
       mbar_init(&o_full[t], 1);
       mbar_init(&o_free[t], 4);
+      mbar_init(&s_free[t], 4);
+      mbar_init(&pv_done[t], 1);
     }
     mbar_init(mma_done, C::MW);
     mbar_init(qt_full, 4 * NQ);
@@ -395,7 +412,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     int last_k[NS], last_v[NS];
 #pragma unroll
     for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
-    int q_last = -1;  // item count of the last Q load issued
+    int q_last[C::QB];  // per Q buffer: item count of the last Q load issued into it
+#pragma unroll
+    for (int b = 0; b < C::QB; ++b) q_last[b] = -1;
     if (lane == 0) {
       const uint64_t pol_q = policy_evict_first();
       // The first item's Q goes out before anything else: after an L2 flush
@@ -412,17 +431,25 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
               tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
                           (w0.qblk * NQ + t) * kTileM, w0.h, w0.b, pol_q);
           q_pre = true;
-          q_last = 0;
+          q_last[0] = 0;
         }
       }
       const uint64_t pol_kv = policy_evict_last();
       const int G = gridDim.x;
       // (with no more items than CTAs there is nothing to hand out: no ticket
       // is drawn and the launcher reserves none)
+      const bool sched_on = PERS && n_items > G && a.sched != nullptr;
+      bool claimed = false;  // this CTA has claimed both words (after its first item's loads went out)
       auto draw = [&]() -> int {
-        if (!PERS || n_items <= G || a.sched == nullptr) return -1;
-        const unsigned long long tk = atomicAdd(a.sched, 1ull);
-        return tk < static_cast<unsigned long long>(n_items - G) ? G + static_cast<int>(tk) : -1;
+        if (!sched_on) return -1;
+        if (!claimed) {
+          claim(a.sched, a.sched_gen);
+          claim(a.sched + 1, a.sched_gen);
+          claimed = true;
+        }
+        unsigned tk = 0;
+        if (!tagged_add(a.sched, a.sched_gen, a.err, &tk)) return -1;
+        return tk < static_cast<unsigned>(n_items - G) ? G + static_cast<int>(tk) : -1;
       };
       int it = 0, na = 0, nr = 0;  // key tiles, active items and ring slots so far
       bool ok = true, drawn_last = false, first = true;
@@ -447,13 +474,15 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         if (q_pre) {
           q_pre = false;  // the first item's Q is already on its way
         } else {
-          if (na > 0 && !mbar_wait(q_free, (na - 1) & 1, ab, SITE_Q_FULL)) break;
-          mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
+          // buffer qb last held item na - QB, whose MMAs (or Q copy) must be done
+          const int qb = na % C::QB;
+          if (na >= C::QB && !mbar_wait(q_free(qb), (na / C::QB - 1) & 1, ab, SITE_Q_FULL)) break;
+          mbar_arrive_expect_tx(&q_full[qb], NQ * C::Q_TILE);
           for (int t = 0; t < NQ; ++t)
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
-                          (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
-          q_last = na;
+              tma_load_4d(&tm_q, &q_full[qb], smem + C::OFF_Q + (qb * NQ + t) * C::Q_TILE + c * C::Q_CHUNK,
+                          c * C::CW, (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
+          q_last[qb] = na;
         }
         for (int j = w.jb; j < w.je_all; ++j, ++it) {
           const int s = it % NS, r = it / NS;
@@ -486,12 +515,17 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
       if (PERS && !drawn_last)
         while (draw() >= 0) {
         }
-      // The last CTA done drawing returns the slot to zero (the fences order
-      // every CTA's last draw before its done count, and the count before
-      // the reset).
-      if (PERS && n_items > G && a.sched != nullptr) {
+      // The last CTA done drawing returns both words to zero (the fences
+      // order every CTA's last draw before its done count, and the count
+      // before the reset).
+      if (sched_on) {
+        if (!claimed) {  // (every path above draws at least once; kept for safety)
+          claim(a.sched, a.sched_gen);
+          claim(a.sched + 1, a.sched_gen);
+        }
         __threadfence();
-        if (atomicAdd(a.sched + 1, 1ull) == static_cast<unsigned long long>(G - 1)) {
+        unsigned done_before = 0;
+        if (tagged_add(a.sched + 1, a.sched_gen, a.err, &done_before) && done_before == static_cast<unsigned>(G - 1)) {
           __threadfence();
           atomicExch(a.sched, 0ull);
           atomicExch(a.sched + 1, 0ull);
@@ -502,7 +536,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     __syncthreads();  // teardown rendezvous
     if (lane == 0 && *abort_flag) {
       // let the copies still in flight land before the CTA's shared memory goes away
-      if (q_last >= 0) mbar_wait_teardown(q_full, q_last & 1);
+      for (int b = 0; b < C::QB; ++b)
+        if (q_last[b] >= 0) mbar_wait_teardown(&q_full[b], (q_last[b] / C::QB) & 1);
       for (int s = 0; s < NS; ++s) {
         if (last_k[s] >= 0) mbar_wait_teardown(&k_full[s], last_k[s] & 1);
         if (last_v[s] >= 0) mbar_wait_teardown(&v_full[s], last_v[s] & 1);
@@ -522,7 +557,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     // another.  An item's first PV into O waits until the previous item's O
     // has been read out (o_free).
     const int m = warp - C::WARP_MMA;
-    if (lane == 0) {
+    // The whole warp runs the loop (barrier waits by every lane, counters kept
+    // by every lane, so the MMA operands are warp-uniform); one elected lane
+    // issues each group of MMAs and its commit.
+    constexpr unsigned FULL = 0xffffffffu;
+    {
       const uint32_t idesc_qk = idesc_make(Elem<T>::ab, kTileM, BN, false, false);
       const uint32_t idesc_pv = idesc_make(Elem<T>::ab, kTileM, D, false, !C::VT);
       // Shared-memory descriptors of the tile bases; the start address field
@@ -533,18 +572,21 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
       const uint64_t dV = C::VT ? sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024)
                                 : sdesc_sw128(smem_u32(smem + C::OFF_V), C::KV_CHUNK, 1024);
       // S_t = Q_t K^T into the S columns of query tile t (K tile at descriptor bK)
-      auto issue_s = [&](int t, uint64_t bK) {
-        const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
+      auto issue_s = [&](int t, uint64_t bK, int qb) {
+        const uint64_t a0 = dQ + (((qb * NQ + t) * C::Q_TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
           const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
           const uint32_t off_k = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
           if constexpr (C::QT)
-            mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + BN + D + kk * 8, bK + off_k, idesc_qk,
+            mma_ts<TF32>(tmem + t * C::TILE_COLS, tmem + t * C::TILE_COLS + C::O_COL + D + kk * 8, bK + off_k, idesc_qk,
                          kk > 0 ? 1u : 0u);
           else
             mma_ss<TF32>(tmem + t * C::TILE_COLS, a0 + off_q, bK + off_k, idesc_qk, kk > 0 ? 1u : 0u);
         }
+      };
+      auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t site) -> bool {
+        return __all_sync(FULL, mbar_wait(bar, parity, ab, site));
       };
       constexpr int TPW = NQ / C::MW;  // query tiles per MMA warp: t = m + tt * MW
       int it = 0, na = 0;
@@ -554,27 +596,30 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
       bool ok = true;
       int taken = -1;
 #pragma unroll 1
-      while (ok) {
+      while (ok && !C::SP) {
         if (!PERS && taken >= 0) break;
-        const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, false);
+        const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, true);
         if (taken < 0) taken = 0;
         if (idx < 0) break;
         int je[NQ];
         const Item w = decode_item<NQ, BN>(a, idx, je);
         if (w.je_all <= w.jb) continue;
-        ok = mbar_wait(C::QT ? qt_full : q_full, na & 1, ab, SITE_Q_FULL) &&
-             mbar_wait(&k_full[it % NS], (it / NS) & 1, ab, SITE_K_FULL);
+        ok = wait_all(C::QT ? qt_full : &q_full[0], na & 1, SITE_Q_FULL) &&
+             wait_all(&k_full[it % NS], (it / NS) & 1, SITE_K_FULL);
         if (!ok) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int tt = 0; tt < TPW; ++tt) {
-          const int t = m + tt * C::MW;
-          if (sel(je, t) > w.jb) {
-            issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4));
-            mma_commit(&s_full[t]);
+          for (int tt = 0; tt < TPW; ++tt) {
+            const int t = m + tt * C::MW;
+            if (sel(je, t) > w.jb) {
+              issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4), 0);
+              mma_commit(&s_full[t]);
+            }
           }
+          if constexpr (!C::KVM) mma_commit(&k_empty[it % NS]);
         }
-        if constexpr (!C::KVM) mma_commit(&k_empty[it % NS]);
+        __syncwarp();
         for (int j = w.jb; ok && j < w.je_all; ++j) {
           const int i = it + (j - w.jb);
           const int s = i % NS, r = i / NS;
@@ -587,32 +632,39 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
             const int t = m + tt * C::MW;
             const int je_t = sel(je, t);
             if (!ok || j >= je_t) continue;
-            ok = mbar_wait(&p_full[t], sp[tt] & 1, ab, SITE_P_FULL);
-            if (ok && j == w.jb && oc[tt] > 0) ok = mbar_wait(&o_free[t], (oc[tt] - 1) & 1, ab, SITE_O_FULL);
-            if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
+            ok = wait_all(&p_full[t], sp[tt] & 1, SITE_P_FULL);
+            if (ok && j == w.jb && oc[tt] > 0) ok = wait_all(&o_free[t], (oc[tt] - 1) & 1, SITE_O_FULL);
+            if (ok && !v_ready) ok = v_ready = wait_all(&v_full[s], r & 1, SITE_V_FULL);
             if (!ok) continue;
             tc_fence_after();
             ++sp[tt];
-            // O_t += P_t V: P from tensor memory; V MN-major (rows = keys), or for
-            // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step)
-            const uint32_t d_o = tmem + t * C::TILE_COLS + BN;
-            const uint32_t p_t = tmem + t * C::TILE_COLS;
+            const bool more = j + 1 < je_t;
+            if (elect_one()) {
+              // O_t += P_t V: P from tensor memory; V MN-major (rows = keys), or for
+              // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step)
+              const uint32_t d_o = tmem + t * C::TILE_COLS + C::O_COL;
+              const uint32_t p_t = tmem + t * C::TILE_COLS + C::P_COL;
 #pragma unroll
-            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-              const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
-                                         : (kk * C::PV_ROWS * 128) >> 4;
-              mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > w.jb || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
+                                           : (kk * C::PV_ROWS * 128) >> 4;
+                mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > w.jb || kk > 0) ? 1u : 0u);
+              }
+              if (!more) mma_commit(&o_full[t]);
             }
-            if (j + 1 < je_t) {
+            __syncwarp();
+            if (more) {
               if (!k_next) {
-                ok = k_next = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+                ok = k_next = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
                 if (!ok) continue;
                 tc_fence_after();
               }
-              issue_s(t, bK);
-              mma_commit(&s_full[t]);
+              if (elect_one()) {
+                issue_s(t, bK, 0);
+                mma_commit(&s_full[t]);
+              }
+              __syncwarp();
             } else {
-              mma_commit(&o_full[t]);
               ++oc[tt];
             }
           }
@@ -620,32 +672,126 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
           if constexpr (C::KVM) {
             // stage j+1 must be seen full by every MMA warp before stage j is
             // freed, which keeps each warp's waits in phase order
-            if (j + 1 < w.je_all && !k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+            if (j + 1 < w.je_all && !k_next) ok = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
             if (!ok) break;
-            mma_commit(&k_empty[s]);
+            if (elect_one()) mma_commit(&k_empty[s]);
+            __syncwarp();
           } else {
-            if (!v_ready) ok = mbar_wait(&v_full[s], r & 1, ab, SITE_V_FULL);
+            if (!v_ready) ok = wait_all(&v_full[s], r & 1, SITE_V_FULL);
             if (!ok) break;
-            mma_commit(&v_empty[s]);
+            if (elect_one()) mma_commit(&v_empty[s]);
+            __syncwarp();
             if (j + 1 < w.je_all) {
-              if (!k_next) ok = mbar_wait(&k_full[sn], rn & 1, ab, SITE_K_FULL);
+              if (!k_next) ok = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
               if (!ok) break;
-              mma_commit(&k_empty[sn]);
+              if (elect_one()) mma_commit(&k_empty[sn]);
+              __syncwarp();
             }
           }
         }
         if (!ok) break;
         // Q in shared memory: free for the next item's load once this item's
         // last QK^T (issued above) has completed
-        if constexpr (!C::QT) mma_commit(q_empty);
+        if constexpr (!C::QT) {
+          if (elect_one()) mma_commit(&q_empty[0]);
+          __syncwarp();
+        }
         it += w.je_all - w.jb;
         ++na;
+      }
+      if constexpr (C::SP) {
+        // SP: one MMA warp per query tile (t = m).  Per key tile j the warp
+        // issues S(j+1) as soon as the softmax has read S(j) into registers
+        // (s_free), then PV(j) once P(j) is written (p_full): the next
+        // scores are computed while the softmax works on these.  P has
+        // columns of its own; pv_done tells the softmax when P and O are
+        // free again.  Every warp waits for and frees every stage of the
+        // item's key range, so the stage phases stay in step.
+        const int t = m;
+        int sn_ = 0, pn = 0, on = 0;  // S tiles issued, P tiles consumed, outputs done (this tile)
+        while (ok) {
+          if (!PERS && taken >= 0) break;
+          const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, true);
+          if (taken < 0) taken = 0;
+          if (idx < 0) break;
+          int je[NQ];
+          const Item w = decode_item<NQ, BN>(a, idx, je);
+          if (w.je_all <= w.jb) continue;
+          const int je_t = sel(je, t);
+          const int qb = na % C::QB;
+          ok = wait_all(C::QT ? qt_full : &q_full[qb], C::QT ? (na & 1) : ((na / C::QB) & 1), SITE_Q_FULL) &&
+               wait_all(&k_full[it % NS], (it / NS) & 1, SITE_K_FULL);
+          if (!ok) break;
+          if (je_t > w.jb) {
+            if (sn_ > 0) ok = wait_all(&s_free[t], (sn_ - 1) & 1, SITE_S_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+              issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4), qb);
+              mma_commit(&s_full[t]);
+            }
+            __syncwarp();
+            ++sn_;
+          }
+          for (int j = w.jb; ok && j < w.je_all; ++j) {
+            const int i = it + (j - w.jb);
+            const int s_ = i % NS;
+            const int sn = (i + 1) % NS, rn = (i + 1) / NS;
+            bool k_next = false;
+            if (j < je_t) {
+              if (j + 1 < je_t) {
+                ok = k_next = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
+                if (ok) ok = wait_all(&s_free[t], (sn_ - 1) & 1, SITE_S_FULL);
+                if (!ok) break;
+                tc_fence_after();
+                if (elect_one()) {
+                  issue_s(t, dK + ((sn * C::KV_TILE) >> 4), qb);
+                  mma_commit(&s_full[t]);
+                }
+                __syncwarp();
+                ++sn_;
+              }
+              ok = wait_all(&p_full[t], pn & 1, SITE_P_FULL);
+              if (ok && j == w.jb && on > 0) ok = wait_all(&o_free[t], (on - 1) & 1, SITE_O_FULL);
+              if (!ok) break;
+              tc_fence_after();
+              ++pn;
+              const bool last = j + 1 == je_t;
+              if (elect_one()) {
+                const uint32_t d_o = tmem + t * C::TILE_COLS + C::O_COL;
+                const uint32_t p_t = tmem + t * C::TILE_COLS + C::P_COL;
+                const uint64_t bV = dV + ((s_ * C::KV_TILE) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                  const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
+                                             : (kk * C::PV_ROWS * 128) >> 4;
+                  mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > w.jb || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&pv_done[t]);
+                if (last) mma_commit(&o_full[t]);
+              }
+              __syncwarp();
+              if (last) ++on;
+            }
+            if (j + 1 < w.je_all && !k_next) ok = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
+            if (!ok) break;
+            if (elect_one()) mma_commit(&k_empty[s_]);
+            __syncwarp();
+          }
+          if (!ok) break;
+          if constexpr (!C::QT) {
+            if (elect_one()) mma_commit(&q_empty[qb]);  // this item's MMAs read Q buffer qb
+            __syncwarp();
+          }
+          it += w.je_all - w.jb;
+          ++na;
+        }
       }
     }
     __syncwarp();
     __syncthreads();  // teardown rendezvous
     if (*abort_flag) {
-      if (lane == 0) {
+      if (elect_one()) {  // the lane that issued this warp's MMAs
         mma_commit(mma_done);  // fires once every MMA warp's issued MMAs have finished
         mbar_wait_teardown(mma_done, 0);
       }
@@ -661,8 +807,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * C::TILE_COLS;
-    const uint32_t tO = tS + BN;
+    const uint32_t tO = tS + C::O_COL;
     int sc = 0, oc = 0, na = 0;  // S tiles, outputs and Q copies so far (barrier phases)
+    int pvc = 0;                 // P tiles written so far (SP: pv_done phases)
     bool ok = true;
     // Copy this thread's Q row of item idx (TF32-rounded by the load for
     // fp32; packed pairs for bf16/fp16) from the swizzled shared tile into
@@ -721,6 +868,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         tc_fence_after();
         uint32_t s[BN];
         load_row<BN>(tS, s);
+        if constexpr (C::SP) {  // S is in registers: the next QK^T may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[t]);
+        }
         const int kv0 = j * BN;
         if (kv0 + BN > kv_lim || (a.causal && kv0 + BN - 1 > q_lo + off)) {
           int lim = kv_lim;
@@ -730,17 +882,16 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= lim) s[c] = f2u(-INFINITY);
         }
-        // row max: 8 independent partial maxima, then a tree (no 128-long
-        // dependency chain)
+        // row max: 8 independent partial maxima, each folding in two columns
+        // per three-input max, then a tree (no 128-long dependency chain)
         float mxa[8];
 #pragma unroll
-        for (int kq = 0; kq < 8; ++kq) mxa[kq] = u2f(s[kq]);
+        for (int kq = 0; kq < 8; ++kq) mxa[kq] = fmaxf(u2f(s[kq]), u2f(s[8 + kq]));
 #pragma unroll
-        for (int c = 8; c < BN; c += 8)
+        for (int c = 16; c < BN; c += 16)
 #pragma unroll
-          for (int kq = 0; kq < 8; ++kq) mxa[kq] = fmaxf(mxa[kq], u2f(s[c + kq]));
-        const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+          for (int kq = 0; kq < 8; ++kq) mxa[kq] = fmax3(mxa[kq], u2f(s[c + kq]), u2f(s[c + 8 + kq]));
+        const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]));
         const float m_new = fmaxf(m_run, mx * a.sl2);
         const bool grow = m_new > m_run + 8.0f;
         float alpha = 1.f;
@@ -750,22 +901,66 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        if constexpr (C::SP) {
+          // P and O are free once the previous PV of this tile completed
+          // (long since, as a rule: it was issued a whole softmax step ago)
+          if (pvc > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (pvc - 1) & 1, ab, SITE_P_FULL));
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
         float rsa[8];  // row sum: 8 independent partial sums
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq) rsa[kq] = 0.f;
+        // P by halves of 64 columns.  TF32, and SP: each half is stored to
+        // tensor memory as soon as it is formed (over S, whose values are all
+        // in registers by now, or into P's own columns with SP), formed in
+        // place in s[] (a word goes to a slot already read).  TF32 rounds to
+        // nearest (ties away) by adding half a TF32 ulp to the bit pattern:
+        // the kind::tf32 product reads only the top 19 bits of each 32-bit
+        // element, P >= 0 and finite, so a carry into the exponent is the
+        // correct rounding (a conversion instruction per element measured
+        // ~1000 cycles a row).
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          // exponent arguments and partial sums two columns per instruction
-          float x0, x1;
-          fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), a.sl2, a.sl2, -m_use, -m_use);
-          // the exponentials may be split between the MUFU unit and the FMA pipe
-          const float p0 = (c & 7) < EMU ? ex2_poly(x0) : ex2_approx(x0);
-          const float p1 = ((c + 1) & 7) < EMU ? ex2_poly(x1) : ex2_approx(x1);
-          float& r0 = rsa[c & 7];
-          float& r1 = rsa[(c & 7) + 1];
-          add2(r0, r1, r0, r1, p0, p1);
-          s[c] = f2u(p0);
-          s[c + 1] = f2u(p1);
+        for (int h = 0; h < BN; h += 64) {
+#pragma unroll
+          for (int c = h; c < h + 64; c += 2) {
+            // exponent arguments and partial sums two columns per instruction
+            float x0, x1;
+            fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), a.sl2, a.sl2, -m_use, -m_use);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            float& r0 = rsa[c & 7];
+            float& r1 = rsa[(c & 7) + 1];
+            add2(r0, r1, r0, r1, p0, p1);
+            if constexpr (TF32) {
+              s[c] = f2u(p0) + 0x1000u;
+              s[c + 1] = f2u(p1) + 0x1000u;
+            } else if constexpr (C::SP) {
+              s[h + (c - h) / 2] = Elem<T>::pack2(p0, p1);
+            } else {
+              s[c] = f2u(p0);
+              s[c + 1] = f2u(p1);
+            }
+          }
+          if constexpr (TF32) {
+            if (h == 0) tmem_st_x64_at<0>(tS + C::P_COL, s);
+            else tmem_st_x64_at<(BN > 64 ? 64 : 0)>(tS + C::P_COL + 64, s);
+          } else if constexpr (C::SP) {
+            if (h == 0) tmem_st_x32_at<0>(tS + C::P_COL, s);
+            else tmem_st_x32_at<(BN > 64 ? 64 : 0)>(tS + C::P_COL + 32, s);
+          }
+        }
+        if constexpr (!TF32 && !C::SP) {
+          // half precision over S: packed once the whole row is formed (by
+          // halves this form measured spills)
+          uint32_t pk[BN / 2];
+#pragma unroll
+          for (int c = 0; c < BN / 2; ++c) pk[c] = Elem<T>::pack2(u2f(s[2 * c]), u2f(s[2 * c + 1]));
+          if constexpr (BN == 128)
+            tmem_st_x64(tS, pk);
+          else
+            tmem_st_x32(tS, pk);
         }
         {
           float a0, a1, b0, b1;
@@ -774,7 +969,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
           add2(a0, a1, a0, a1, b0, b1);
           l += a0 + a1;
         }
-        store_p<T, BN>(tS, s);
         // O was produced by PV of earlier tiles: rescale it to the new max.  The
         // tensor-memory loads/stores are warp-collective, so the warp rescales
         // together when any of its rows grew (alpha is 1 for the others).
@@ -792,6 +986,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[t]);
+        ++pvc;
       }
       if (!ok) break;
       // The next item's Q goes into tensor memory before this item's output
@@ -896,11 +1091,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, EMU, PERS>::THREADS, 1)
   }
 }
 
-template <typename T, int D, int NQ, int BN, int NS, int EMU, bool PERS>
+template <typename T, int D, int NQ, int BN, int NS, bool SP, bool PERS>
 cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& b,
                         int grid, cudaStream_t st) {
-  using C = Cfg<T, D, NQ, BN, NS, EMU, PERS>;
-  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, EMU, PERS>;
+  using C = Cfg<T, D, NQ, BN, NS, SP, PERS>;
+  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, SP, PERS>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -911,12 +1106,13 @@ cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, b);
+  return launch_pdl("attn_fwd_kernel", kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, b);
 }
 
-// One CTA per item when the items fit on the SMs at once; otherwise the
+// One CTA per item when the items fit on the SMs at once, or when there are
+// no ticket words (a launch without workspace for them); otherwise the
 // persistent form on every SM, drawing items by ticket.
-template <typename T, int D, int NQ, int BN, int NS, int EMU>
+template <typename T, int D, int NQ, int BN, int NS, bool SP>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                        int splits, cudaStream_t st) {
   int dev = 0, sms = 0;
@@ -926,24 +1122,15 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(a.num_qblk) * a.B * a.H * splits;
   if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   AttnArgs b = a;
   b.splits = splits;
-  if (items <= sms) return launch_form<T, D, NQ, BN, NS, EMU, false>(tq, tk, tv, b, static_cast<int>(items), st);
-  e = counter_slot(&b.sched);
-  if (e != cudaSuccess) return e;
-  return launch_form<T, D, NQ, BN, NS, EMU, true>(tq, tk, tv, b, sms, st);
+  if (items <= sms || a.sched == nullptr)
+    return launch_form<T, D, NQ, BN, NS, SP, false>(tq, tk, tv, b, static_cast<int>(items), st);
+  return launch_form<T, D, NQ, BN, NS, SP, true>(tq, tk, tv, b, sms, st);
 }
 
 }  // namespace
-
-#ifndef LA_EMU_D64
-#define LA_EMU_D64 0
-#endif
-#ifndef LA_EMU_D128
-#define LA_EMU_D128 0
-#endif
-constexpr int kEmuD64 = LA_EMU_D64;
-constexpr int kEmuD128 = LA_EMU_D128;
 
 // Launch shapes per (dtype, D): query rows per CTA = 128 * NQ, key tile BN,
 // stages NS; chosen so Q + NS stages of K and V fit in 227 KB of shared memory
@@ -963,19 +1150,20 @@ bool attn_shape(la_dtype dt, int D, AttnShape* s) {
 
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnArgs& a, int splits, cudaStream_t st) {
-  // EMU: share of the exponentials on the FMA pipe (eighths).  Measured on
-  // GB300: every share above 0 was slower (the MUFU unit is not the limit:
-  // ncu shows the XU pipe about 20% busy), so it is 0.
+  // SP (P in columns of its own, the next QK^T during this softmax) measured
+  // slower everywhere so far: half precision D=64 (bound by its softmax) 4%,
+  // fp32 D=64 on 64-key tiles (the only fp32 tile that leaves room for P)
+  // 37%, its N=64 QK^T products costing more than the overlap saves.
   switch (dt) {
     case LA_BF16:
-      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3, kEmuD64>(tq, tk, tv, a, splits, st)
-                     : launch_one<__nv_bfloat16, 128, 2, 128, 2, kEmuD128>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3, false>(tq, tk, tv, a, splits, st)
+                     : launch_one<__nv_bfloat16, 128, 2, 128, 2, false>(tq, tk, tv, a, splits, st);
     case LA_F16:
-      return D == 64 ? launch_one<__half, 64, 2, 128, 3, kEmuD64>(tq, tk, tv, a, splits, st)
-                     : launch_one<__half, 128, 2, 128, 2, kEmuD128>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<__half, 64, 2, 128, 3, false>(tq, tk, tv, a, splits, st)
+                     : launch_one<__half, 128, 2, 128, 2, false>(tq, tk, tv, a, splits, st);
     case LA_F32:
-      return D == 64 ? launch_one<float, 64, 2, 128, 2, kEmuD64>(tq, tk, tv, a, splits, st)
-                     : launch_one<float, 128, 1, 64, 2, 0>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<float, 64, 2, 128, 2, false>(tq, tk, tv, a, splits, st)
+                     : launch_one<float, 128, 1, 64, 2, false>(tq, tk, tv, a, splits, st);
   }
   return cudaErrorInvalidValue;
 }

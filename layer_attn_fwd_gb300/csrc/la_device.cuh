@@ -255,6 +255,20 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
   }
 }
+// One lane of a converged warp (the same lane every time the whole warp is
+// active): the issuing thread of the tcgen05 MMAs and commits.  The loop
+// around the issue runs on the whole warp, so that the operands are
+// warp-uniform; measured on GB300, an MMA loop run by one lane alone (inside
+// `if (lane == 0)`) issued a step of 12 MMAs in ~1030 cycles against ~650
+// for the same loop on the whole warp with an elected issuer.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrive once on the mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -318,6 +332,15 @@ __device__ __forceinline__ void tmem_st_x64(uint32_t taddr, const uint32_t (&v)[
                : "memory");
 }
 
+// Store columns [OFF, OFF + 32) of a register row (no copy of the row).
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_st_x32_at(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(OFF + 32 <= N, "row slice");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               :: "r"(taddr), "r"(v[OFF + 0]), "r"(v[OFF + 1]), "r"(v[OFF + 2]), "r"(v[OFF + 3]), "r"(v[OFF + 4]), "r"(v[OFF + 5]), "r"(v[OFF + 6]), "r"(v[OFF + 7]), "r"(v[OFF + 8]), "r"(v[OFF + 9]), "r"(v[OFF + 10]), "r"(v[OFF + 11]), "r"(v[OFF + 12]), "r"(v[OFF + 13]), "r"(v[OFF + 14]), "r"(v[OFF + 15]), "r"(v[OFF + 16]), "r"(v[OFF + 17]), "r"(v[OFF + 18]), "r"(v[OFF + 19]), "r"(v[OFF + 20]), "r"(v[OFF + 21]), "r"(v[OFF + 22]), "r"(v[OFF + 23]), "r"(v[OFF + 24]), "r"(v[OFF + 25]), "r"(v[OFF + 26]), "r"(v[OFF + 27]), "r"(v[OFF + 28]), "r"(v[OFF + 29]), "r"(v[OFF + 30]), "r"(v[OFF + 31])
+               : "memory");
+}
+
 // Store columns [OFF, OFF + 64) of a register row (no copy of the row).
 template <int OFF, int N>
 __device__ __forceinline__ void tmem_st_x64_at(uint32_t taddr, const uint32_t (&v)[N]) {
@@ -335,23 +358,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x on the FMA pipe (to take part of the exponentials off the MUFU unit).
-// x = n + f with n = round(x), read from the low mantissa bits of x + 1.5*2^23,
-// and f in [-1/2, 1/2]; 2^f comes from a degree-3 polynomial fitted for this
-// file by a Remez exchange on relative error over [-1/2, 1/2] (max relative
-// error 7.5e-5, about 13.7 bits, finer than the bf16/fp16/tf32 rounding P gets
-// before the PV product); 2^n is added straight into the exponent field.
-// Valid for x <= 64; x < -125 (including -inf, a masked score) returns 0.
-__device__ __forceinline__ float ex2_poly(float x) {
-  const float xc = fmaxf(x, -125.0f);
-  const float t = __fadd_rn(xc, 12582912.0f);
-  const float n = __fsub_rn(t, 12582912.0f);
-  const float f = __fsub_rn(xc, n);
-  float p = fmaf(0.05517167f, f, 0.24261113f);
-  p = fmaf(p, f, 0.69326097f);
-  p = fmaf(p, f, 0.99992806f);
-  const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-  return x < -125.0f ? 0.0f : r;
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction for two

@@ -16,12 +16,22 @@
 
 namespace la {
 
-// Launch with programmatic stream serialization: the grid may be scheduled
-// while the previous grid in the stream is still running; it must call
-// pdl_wait() before touching memory that grid produces or consumes.
+// Per-launch timing (la_profile_start / la_profile_stop): when on, every
+// launch is bracketed by two CUDA events on its stream.  Both are no-ops
+// otherwise.  prof_on(): recording is on (launches then run without
+// programmatic serialization, so that no kernel overlaps the events of the
+// one before it).
+void prof_before(cudaStream_t st, const char* name);
+void prof_after(cudaStream_t st);
+bool prof_on();
+
+// Every kernel of the library is launched here.  pdl: with programmatic
+// stream serialization, so the grid may be scheduled while the previous grid
+// in the stream is still running; it must call pdl_wait() before touching
+// memory that grid produces or consumes.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
+cudaError_t launch(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                   bool pdl, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -31,8 +41,16 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  cfg.numAttrs = (pdl && !prof_on()) ? 1 : 0;
+  prof_before(st, name);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  prof_after(st);
+  return e;
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  return launch(name, kern, grid, block, smem, st, true, static_cast<Args&&>(args)...);
 }
 
 // Rows of one query tile (the M of every tcgen05 MMA here).
@@ -51,7 +69,8 @@ struct AttnArgs {
   int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
   int tiles_per_split;        // key tiles handled by one split
   int splits;                 // key-range splits (set by the launcher)
-  unsigned long long* sched;  // work-item ticket counter and done count (set by the launcher)
+  unsigned long long* sched;  // persistent form: ticket word and done word, in the caller's workspace
+  unsigned sched_gen;         // this launch's tag in the high half of both words (never 0)
   uint32_t* err;              // device error word
   int skip_loads;             // test hook: issue no TMA load, so every wait runs out
 #if LA_CHECKED
@@ -70,16 +89,12 @@ struct AttnShape {
 };
 bool attn_shape(la_dtype dt, int D, AttnShape* s);
 
-// Launch the persistent attention kernel over its num_qblk * B*H * splits
-// work items (one CTA per SM, at most one per item).
+// Launch the attention kernel over its num_qblk * B*H * splits work items:
+// one CTA per item when they fit on the SMs at once, or when a.sched is null
+// (no workspace for the ticket words); otherwise the persistent form, one
+// CTA per SM drawing items by ticket from a.sched.
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const AttnArgs& a, int splits, cudaStream_t st);
-
-// A slot of the device's attention work-ticket counters: ctr[0] the tickets
-// drawn, ctr[1] the CTAs done drawing.  Both are zero when a launch starts
-// and when it ends, so a launch captured in a CUDA graph can be replayed; a
-// graph must not be replayed on two streams at the same time.
-cudaError_t counter_slot(unsigned long long** ctr);
 
 // Merge split partials into o.
 struct CombineArgs {
@@ -105,9 +120,11 @@ cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, 
                                int R, int C, cudaStream_t st, bool pdl = false);
 
 // LayerNorm of M rows of d elements (d a multiple of 64, 16-byte aligned
-// pointers), statistics in fp32.  pdl: as for launch_transpose32.
+// pointers), statistics in fp32.  pdl: as for launch_transpose32.  With
+// stats non-null only the row statistics (mean, 1 / sqrt(var + eps)) are
+// written there (y is not touched).
 cudaError_t launch_layernorm(la_dtype dt, const void* x, const void* gamma, const void* beta, void* y, long long M,
-                             int d, float eps, cudaStream_t st, bool pdl = false);
+                             int d, float eps, cudaStream_t st, bool pdl = false, float2* stats = nullptr);
 
 // Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`.
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
@@ -125,6 +142,11 @@ struct ProjArgs {
   uint32_t* err;
   int v_transposed;   // write V as V^T [B, H, D, S_pad] (fp32 sublayer) instead of [B, H, S, D]
   long long S_pad;    // row length of V^T
+  // LayerNorm in front (the pre-norm block), or all null: per-row (mean,
+  // 1 / sqrt(var + eps)) [M] and gamma, beta [K]; x is then the raw input
+  const float2* ln_stats;
+  const void* ln_gamma;
+  const void* ln_beta;
 #if LA_CHECKED
   long long qk_elems; // elements of each of q and k
   long long v_elems;  // elements of v, or of V^T

@@ -14,16 +14,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <mutex>
-
 #include "la_device.cuh"
 #include "la_internal.h"
-
-// The attention's work-ticket counters: per slot a ticket count and a count
-// of CTAs done drawing, both zero between launches (the last CTA of a launch
-// to finish drawing resets them).  Launches take the slots in turn, so that
-// launches that may run at the same time (on other streams) rarely share one.
-__device__ unsigned long long la_counters[2 * 64];
 
 namespace la {
 namespace {
@@ -228,10 +220,13 @@ __device__ __forceinline__ float group_sum(float v) {
 // output is formed.  Longer rows take three passes (the later two hit L1).
 // Every lane of a warp runs the same number of loop trips (rows past the end
 // skip their loads and stores), so the group sums see whole warps.
-template <typename T, int FPL, int LPR>
+// STATS: only the row statistics (mean, 1 / sqrt(var + eps)) are written, to
+// stats[row], for a projection that normalises its input tiles as it loads
+// them; the arithmetic of the statistics is the same.
+template <typename T, int FPL, int LPR, bool STATS>
 __global__ void __launch_bounds__(256, 3)
     layernorm_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
-                     T* __restrict__ y, long long M, int d, float eps) {
+                     T* __restrict__ y, float2* __restrict__ stats, long long M, int d, float eps) {
   using V = Vec16<T>;
   constexpr int E = V::N;
   constexpr int NVL = FPL / E;  // 16-byte vectors a lane holds
@@ -277,6 +272,10 @@ __global__ void __launch_bounds__(256, 3)
             q = fmaf(v[j][e], v[j][e], q);
           }
       const float rstd = 1.f / sqrtf(group_sum<LPR>(q) * inv_d + eps);
+      if constexpr (STATS) {
+        if (live && lane == 0) stats[r] = make_float2(mu, rstd);
+        continue;
+      }
 #pragma unroll
       for (int j = 0; j < NVL; ++j) {
         const int i = lane + LPR * j;
@@ -308,6 +307,10 @@ __global__ void __launch_bounds__(256, 3)
         }
       }
       const float rstd = 1.f / sqrtf(group_sum<LPR>(q) * inv_d + eps);
+      if constexpr (STATS) {
+        if (live && lane == 0) stats[r] = make_float2(mu, rstd);
+        continue;
+      }
       for (int i = lane; i < nv && live; i += LPR) {
         float g[E], b[E];
         V::unpack(xr[i], v);
@@ -334,28 +337,6 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t counter_slot(unsigned long long** ctr) {
-  constexpr int kDev = 64, kSlots = 64;
-  static std::mutex mu;
-  static unsigned long long* addr[kDev] = {};
-  static int next_slot[kDev] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kDev) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, la_counters);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<unsigned long long*>(p);
-  }
-  const int slot = next_slot[dev];
-  next_slot[dev] = (slot + 1) % kSlots;
-  *ctr = addr[dev] + 2 * slot;
-  return cudaSuccess;
-}
-
 cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
   const long long total = static_cast<long long>(a.B) * a.H * a.S_q * (a.D / 4);
   if (total == 0) return cudaSuccess;
@@ -363,12 +344,11 @@ cudaError_t launch_combine(la_dtype dt, const CombineArgs& a, cudaStream_t st) {
   const int cap = sm_count() * 8;
   const int grid = static_cast<int>(want < cap ? want : cap);
   switch (dt) {
-    case LA_F32: combine_kernel<float><<<grid, 256, 0, st>>>(a); break;
-    case LA_BF16: combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a); break;
-    case LA_F16: combine_kernel<__half><<<grid, 256, 0, st>>>(a); break;
+    case LA_F32: return launch("combine_kernel", combine_kernel<float>, dim3(grid), dim3(256), 0, st, false, a);
+    case LA_BF16: return launch("combine_kernel", combine_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, false, a);
+    case LA_F16: return launch("combine_kernel", combine_kernel<__half>, dim3(grid), dim3(256), 0, st, false, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, long long ld_dst, long long batches,
@@ -381,9 +361,8 @@ cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, 
   dim3 grid((R + 63) / 64, (C + 63) / 64, static_cast<unsigned>(batches));
   const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
   uint32_t* d = reinterpret_cast<uint32_t*>(dst);
-  if (pdl) return launch_pdl(transpose32_kernel, grid, dim3(256), 0, st, s, d, R, C, ld_dst, src_batch, dst_batch, vec);
-  transpose32_kernel<<<grid, 256, 0, st>>>(s, d, R, C, ld_dst, src_batch, dst_batch, vec);
-  return cudaGetLastError();
+  return launch("transpose32_kernel", transpose32_kernel, grid, dim3(256), 0, st, pdl, s, d, R, C, ld_dst, src_batch,
+                dst_batch, vec);
 }
 
 // Row values each lane keeps in registers (within 80 registers, so three
@@ -392,8 +371,8 @@ cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, 
 constexpr int kLnFloatsPerLaneF32 = 16, kLnFloatsPerLaneHalf = 32;
 
 template <typename T, int FPL>
-cudaError_t launch_ln(const void* x, const void* gamma, const void* beta, void* y, long long M, int d, float eps,
-                      cudaStream_t st, bool pdl) {
+cudaError_t launch_ln(const void* x, const void* gamma, const void* beta, void* y, float2* stats, long long M, int d,
+                      float eps, cudaStream_t st, bool pdl) {
   // Half a warp per row when the row fits in registers that way: twice the
   // rows per warp, so a launch of a few thousand rows runs in one wave.
   const bool half_warp = d / Vec16<T>::N <= 16 * (FPL / Vec16<T>::N);
@@ -405,19 +384,22 @@ cudaError_t launch_ln(const void* x, const void* gamma, const void* beta, void* 
   const T* gg = static_cast<const T*>(gamma);
   const T* bb = static_cast<const T*>(beta);
   T* yy = static_cast<T*>(y);
-  auto k = half_warp ? layernorm_kernel<T, FPL, 16> : layernorm_kernel<T, FPL, 32>;
-  if (pdl) return launch_pdl(k, grid, dim3(256), 0, st, xx, gg, bb, yy, M, d, eps);
-  k<<<grid, 256, 0, st>>>(xx, gg, bb, yy, M, d, eps);
-  return cudaGetLastError();
+  if (stats != nullptr) {
+    auto k = half_warp ? layernorm_kernel<T, FPL, 16, true> : layernorm_kernel<T, FPL, 32, true>;
+    return launch("layernorm_stats_kernel", k, grid, dim3(256), 0, st, pdl, xx, gg, bb, yy, stats, M, d, eps);
+  }
+  auto k = half_warp ? layernorm_kernel<T, FPL, 16, false> : layernorm_kernel<T, FPL, 32, false>;
+  return launch("layernorm_kernel", k, grid, dim3(256), 0, st, pdl, xx, gg, bb, yy, stats, M, d, eps);
 }
 
 cudaError_t launch_layernorm(la_dtype dt, const void* x, const void* gamma, const void* beta, void* y, long long M,
-                             int d, float eps, cudaStream_t st, bool pdl) {
+                             int d, float eps, cudaStream_t st, bool pdl, float2* stats) {
   if (M == 0) return cudaSuccess;
   switch (dt) {
-    case LA_F32: return launch_ln<float, kLnFloatsPerLaneF32>(x, gamma, beta, y, M, d, eps, st, pdl);
-    case LA_BF16: return launch_ln<__nv_bfloat16, kLnFloatsPerLaneHalf>(x, gamma, beta, y, M, d, eps, st, pdl);
-    case LA_F16: return launch_ln<__half, kLnFloatsPerLaneHalf>(x, gamma, beta, y, M, d, eps, st, pdl);
+    case LA_F32: return launch_ln<float, kLnFloatsPerLaneF32>(x, gamma, beta, y, stats, M, d, eps, st, pdl);
+    case LA_BF16:
+      return launch_ln<__nv_bfloat16, kLnFloatsPerLaneHalf>(x, gamma, beta, y, stats, M, d, eps, st, pdl);
+    case LA_F16: return launch_ln<__half, kLnFloatsPerLaneHalf>(x, gamma, beta, y, stats, M, d, eps, st, pdl);
   }
   return cudaErrorInvalidValue;
 }
@@ -431,12 +413,10 @@ cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, 
   const int cap = sm_count() * 4;
   dim3 grid(static_cast<unsigned>(want < cap ? want : cap), 2);
   const long long row_bytes = static_cast<long long>(D) * elem_bytes;
-  kv_append_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(k_src),
-                                         reinterpret_cast<const uint4*>(v_src), reinterpret_cast<uint8_t*>(k_dst),
-                                         reinterpret_cast<uint8_t*>(v_dst), n_vec, vec_per_row, rows,
-                                         static_cast<long long>(S_max) * row_bytes,
-                                         static_cast<long long>(at) * row_bytes);
-  return cudaGetLastError();
+  return launch("kv_append_kernel", kv_append_kernel, grid, dim3(256), 0, st, false,
+                reinterpret_cast<const uint4*>(k_src), reinterpret_cast<const uint4*>(v_src),
+                reinterpret_cast<uint8_t*>(k_dst), reinterpret_cast<uint8_t*>(v_dst), n_vec, vec_per_row, rows,
+                static_cast<long long>(S_max) * row_bytes, static_cast<long long>(at) * row_bytes);
 }
 
 }  // namespace la

@@ -18,10 +18,19 @@
 //                 ring.  bf16/fp16 read Wqkv itself (rows = K, columns = N:
 //                 an MN-major operand).  TF32 products take K-major operands
 //                 only, so fp32 reads Wqkv^T [3d, d], transposed beforehand.
-//   warp 5        one thread issues the MMAs; commits free the stages.
+//   warp 5        issues the MMAs (the warp runs the loop, one elected lane
+//                 issues); commits free the stages.
 //   warps 0..3    epilogue, thread r owns row r of the tile.
+//   warps 6..9    (LN form only) LayerNorm in front of the projection
+//                 ("Shape-Aware Attention", section What's next: fusing
+//                 LayerNorm): thread r normalises row r of each x stage in
+//                 shared memory, (x - mean_r) * rstd_r * gamma + beta with the
+//                 row statistics of a stats pre-pass, rounds it to the
+//                 operand type and hands the stage to the MMA warp, so the
+//                 normalised activations never go through global memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <string.h>
 
 #include "la_device.cuh"
 #include "la_internal.h"
@@ -64,9 +73,10 @@ struct PElem<float> {
   }
 };
 
-template <typename T, int BNP_, int NSP_>
+template <typename T, int BNP_, int NSP_, bool LN_ = false>
 struct PCfg {
   static constexpr int BNP = BNP_, NSP = NSP_;
+  static constexpr bool LN = LN_;
   static constexpr int E = sizeof(T);
   static constexpr int CW = 128 / E;           // elements per 128-byte row = K per stage
   static constexpr int A_STAGE = kTileM * 128; // x tile: 128 rows x 128 bytes
@@ -79,14 +89,14 @@ struct PCfg {
   static constexpr int OFF_STG = OFF_B + NSP * B_STAGE;
   static constexpr int OFF_BIAS = OFF_STG + 4 * STG_BYTES;  // each epilogue warp's bias slice (fp32)
   static constexpr int OFF_BAR = OFF_BIAS + 4 * BNP * 4;
-  // full[NSP], empty[NSP], acc_full[2], acc_empty[2], mma_done
-  static constexpr int NBAR = 2 * NSP + 5;
+  // full[NSP], empty[NSP], acc_full[2], acc_empty[2], mma_done, (LN) xf_full[NSP]
+  static constexpr int NBAR = 2 * NSP + 5 + (LN ? NSP : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TMEM_COLS = 2 * BNP <= 256 ? 256 : 512;  // two accumulators (power of two)
   static constexpr int ROWS_PER_KSTEP = 32 / E;  // K rows consumed by one MMA
-  static constexpr int THREADS = 192;
-  static constexpr int WARP_TMA = 4, WARP_MMA = 5;
+  static constexpr int THREADS = LN ? 320 : 192;
+  static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_XF = 6;
   static_assert(BNP % CW == 0 && BNP >= 32 && BNP <= 256 && BNP % 16 == 0, "tile width");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -107,11 +117,59 @@ __device__ __forceinline__ uint4 pack_unit(const float* v, int u) {
   }
 }
 
-template <typename T, int BNP, int NSP>
-__global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
+// 16 bytes of x (CW / 8 values) normalised: (x - mu) * rs * gamma + beta,
+// the LayerNorm kernel's arithmetic, rounded to the operand type (fp32: to
+// TF32 to nearest, ties away, by adding half a TF32 ulp to the bit pattern;
+// the kind::tf32 product reads only the top 19 bits; the copy into shared
+// memory left x unrounded).
+template <typename T>
+__device__ __forceinline__ uint4 ln_unit(uint4 w, const T* gamma, const T* beta, int col, float mu, float rs);
+template <>
+__device__ __forceinline__ uint4 ln_unit<float>(uint4 w, const float* gamma, const float* beta, int col, float mu,
+                                                float rs) {
+  const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + col));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(beta + col));
+  uint4 o;
+  o.x = __float_as_uint(fmaf((__uint_as_float(w.x) - mu) * rs, g.x, b.x)) + 0x1000u;
+  o.y = __float_as_uint(fmaf((__uint_as_float(w.y) - mu) * rs, g.y, b.y)) + 0x1000u;
+  o.z = __float_as_uint(fmaf((__uint_as_float(w.z) - mu) * rs, g.z, b.z)) + 0x1000u;
+  o.w = __float_as_uint(fmaf((__uint_as_float(w.w) - mu) * rs, g.w, b.w)) + 0x1000u;
+  return o;
+}
+template <typename T>
+__device__ __forceinline__ uint4 ln_unit_half(uint4 w, const T* gamma, const T* beta, int col, float mu, float rs) {
+  const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gamma + col));
+  const uint4 bw = __ldg(reinterpret_cast<const uint4*>(beta + col));
+  const uint32_t xs[4] = {w.x, w.y, w.z, w.w}, gs[4] = {gw.x, gw.y, gw.z, gw.w}, bs[4] = {bw.x, bw.y, bw.z, bw.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    T x2[2], g2[2], b2[2];
+    memcpy(x2, &xs[i], 4);
+    memcpy(g2, &gs[i], 4);
+    memcpy(b2, &bs[i], 4);
+    const float y0 = fmaf((static_cast<float>(x2[0]) - mu) * rs, static_cast<float>(g2[0]), static_cast<float>(b2[0]));
+    const float y1 = fmaf((static_cast<float>(x2[1]) - mu) * rs, static_cast<float>(g2[1]), static_cast<float>(b2[1]));
+    o[i] = PElem<T>::pack2(y0, y1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+template <>
+__device__ __forceinline__ uint4 ln_unit<__nv_bfloat16>(uint4 w, const __nv_bfloat16* gamma,
+                                                        const __nv_bfloat16* beta, int col, float mu, float rs) {
+  return ln_unit_half<__nv_bfloat16>(w, gamma, beta, col, mu, rs);
+}
+template <>
+__device__ __forceinline__ uint4 ln_unit<__half>(uint4 w, const __half* gamma, const __half* beta, int col, float mu,
+                                                 float rs) {
+  return ln_unit_half<__half>(w, gamma, beta, col, mu, rs);
+}
+
+template <typename T, int BNP, int NSP, bool LN>
+__global__ void __launch_bounds__(PCfg<T, BNP, NSP, LN>::THREADS, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const ProjArgs a) {
-  using C = PCfg<T, BNP, NSP>;
+  using C = PCfg<T, BNP, NSP, LN>;
   constexpr bool TF32 = PElem<T>::tf32;
   constexpr int CW = C::CW;
   extern __shared__ uint8_t smem_raw[];
@@ -121,6 +179,7 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
   uint64_t* acc_full = empty + NSP;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
+  uint64_t* xf_full = mma_done + 1;  // (LN) stage s normalised in place, ready for the MMAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -139,6 +198,8 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
       mbar_init(&acc_empty[b], 4);  // one arrive per epilogue warp
     }
     mbar_init(mma_done, 1);
+    if constexpr (LN)
+      for (int s = 0; s < NSP; ++s) mbar_init(&xf_full[s], 4);  // one arrive per transform warp
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -197,7 +258,9 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == C::WARP_MMA) {
-    if (lane == 0) {
+    // The whole warp runs the loop and waits (warp-uniform MMA operands); one
+    // elected lane issues the MMAs and their commits.
+    {
       const uint32_t idesc = idesc_make(PElem<T>::ab, kTileM, BNP, false, !C::KMAJ);
       const uint32_t sA = smem_u32(smem + C::OFF_A);
       const uint32_t sB = smem_u32(smem + C::OFF_B);
@@ -205,30 +268,43 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++lt) {
         const int accb = lt & 1, use = lt >> 1;
-        if (use > 0 && !mbar_wait(&acc_empty[accb], (use - 1) & 1, ab, SITE_PROJ_ACC_FREE)) { ok = false; break; }
+        if (use > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&acc_empty[accb], (use - 1) & 1, ab, SITE_PROJ_ACC_FREE))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d = tmem + accb * BNP;
         for (int kt = 0; kt < n_k; ++kt, ++it) {
           const int s = it % NSP, r = it / NSP;
-          if (!mbar_wait(&full[s], r & 1, ab, SITE_PROJ_FULL)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(sA + s * C::A_STAGE + kk * 32, 16, 1024);
-            const uint64_t bd =
-                C::KMAJ ? sdesc_sw128(sB + s * C::B_STAGE + kk * 32, 16, 1024)
-                      : sdesc_sw128(sB + s * C::B_STAGE + kk * C::ROWS_PER_KSTEP * 128, C::B_CHUNK, 1024);
-            mma_ss<TF32>(d, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          if (!__all_sync(0xffffffffu, mbar_wait(LN ? &xf_full[s] : &full[s], r & 1, ab, SITE_PROJ_FULL))) {
+            ok = false;
+            break;
           }
-          mma_commit(&empty[s]);
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(sA + s * C::A_STAGE + kk * 32, 16, 1024);
+              const uint64_t bd =
+                  C::KMAJ ? sdesc_sw128(sB + s * C::B_STAGE + kk * 32, 16, 1024)
+                          : sdesc_sw128(sB + s * C::B_STAGE + kk * C::ROWS_PER_KSTEP * 128, C::B_CHUNK, 1024);
+              mma_ss<TF32>(d, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&empty[s]);
+          }
+          __syncwarp();
         }
-        if (ok) mma_commit(&acc_full[accb]);
+        if (ok) {
+          if (elect_one()) mma_commit(&acc_full[accb]);
+          __syncwarp();
+        }
       }
     }
     __syncwarp();
     __syncthreads();
     if (*abort_flag) {
-      if (lane == 0) {
+      if (elect_one()) {  // the lane that issued the MMAs
         mma_commit(mma_done);
         mbar_wait_teardown(mma_done, 0);
       }
@@ -236,6 +312,44 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
     }
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  } else if (LN && warp >= C::WARP_XF) {
+    // LayerNorm of each x stage in place (LN form).  Thread r owns row r of
+    // the stage; its 128 bytes are eight 16-byte units stored at unit
+    // position u ^ (r % 8) (the 128-byte swizzle the copy wrote).
+    const int xr = (warp - C::WARP_XF) * 32 + lane;
+    const T* gamma = reinterpret_cast<const T*>(a.ln_gamma);
+    const T* beta = reinterpret_cast<const T*>(a.ln_beta);
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const int m = (t / n_tn) * kTileM + xr;
+      float mu = 0.f, rs = 0.f;  // rows past the end (zero-filled) become beta; they are never stored
+      if (m < a.M) {
+        const float2 st = a.ln_stats[m];
+        mu = st.x;
+        rs = st.y;
+      }
+      for (int kt = 0; kt < n_k; ++kt, ++it) {
+        const int s = it % NSP, r = it / NSP;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], r & 1, ab, SITE_PROJ_FULL))) { ok = false; break; }
+        const uint32_t line = smem_u32(smem + C::OFF_A + s * C::A_STAGE) + xr * 128;
+        // all eight loads first, then the arithmetic, then the stores (the
+        // shared-memory accesses are ordered asm statements: interleaving
+        // them unit by unit would serialise their latencies)
+        uint4 xv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) xv[u] = lds128(line + ((u ^ (xr & 7)) << 4));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) xv[u] = ln_unit<T>(xv[u], gamma, beta, kt * CW + u * (CW / 8), mu, rs);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sts128(line + ((u ^ (xr & 7)) << 4), xv[u]);
+        fence_proxy_async_smem();  // the tensor cores read the stage through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xf_full[s]);
+      }
+    }
+    __syncwarp();
+    __syncthreads();
   } else {
     // epilogue: thread owns row warp*32 + lane of the tile.  Per 128-byte
     // column chunk (CW columns, inside one head of one of q/k/v): TMEM ->
@@ -341,10 +455,10 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP>::THREADS, 1)
   }
 }
 
-template <typename T, int BNP, int NSP>
+template <typename T, int BNP, int NSP, bool LN>
 cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a, cudaStream_t st) {
-  using C = PCfg<T, BNP, NSP>;
-  auto kern = qkv_proj_kernel<T, BNP, NSP>;
+  using C = PCfg<T, BNP, NSP, LN>;
+  auto kern = qkv_proj_kernel<T, BNP, NSP, LN>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -361,7 +475,13 @@ cudaError_t launch_p(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArg
   const long long tiles =
       static_cast<long long>((a.N + BNP - 1) / BNP) * ((a.M + kTileM - 1) / kTileM);
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tx, tw, a);
+  return launch_pdl(LN ? "qkv_proj_ln_kernel" : "qkv_proj_kernel", kern, dim3(grid), dim3(C::THREADS),
+                    C::SMEM_BYTES, st, tx, tw, a);
+}
+
+template <typename T, int BNP, int NSP>
+cudaError_t launch_p2(const CUtensorMap& tx, const CUtensorMap& tw, const ProjArgs& a, cudaStream_t st) {
+  return a.ln_stats != nullptr ? launch_p<T, BNP, NSP, true>(tx, tw, a, st) : launch_p<T, BNP, NSP, false>(tx, tw, a, st);
 }
 
 }  // namespace
@@ -394,9 +514,9 @@ cudaError_t launch_proj(la_dtype dt, int block_n, const CUtensorMap& tx, const C
   if (!narrow && block_n != (dt == LA_F32 ? 192 : 256)) return cudaErrorInvalidValue;
   switch (dt) {
     case LA_BF16:
-      return narrow ? launch_p<__nv_bfloat16, 128, 6>(tx, tw, a, st) : launch_p<__nv_bfloat16, 256, 4>(tx, tw, a, st);
-    case LA_F16: return narrow ? launch_p<__half, 128, 6>(tx, tw, a, st) : launch_p<__half, 256, 4>(tx, tw, a, st);
-    case LA_F32: return narrow ? launch_p<float, 128, 6>(tx, tw, a, st) : launch_p<float, 192, 5>(tx, tw, a, st);
+      return narrow ? launch_p2<__nv_bfloat16, 128, 6>(tx, tw, a, st) : launch_p2<__nv_bfloat16, 256, 4>(tx, tw, a, st);
+    case LA_F16: return narrow ? launch_p2<__half, 128, 6>(tx, tw, a, st) : launch_p2<__half, 256, 4>(tx, tw, a, st);
+    case LA_F32: return narrow ? launch_p2<float, 128, 6>(tx, tw, a, st) : launch_p2<float, 192, 5>(tx, tw, a, st);
     default: return cudaErrorInvalidValue;
   }
 }

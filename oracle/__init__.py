@@ -64,6 +64,8 @@ def _load():
             lib.oracle_widen.argtypes = [P, I, LL]
             lib.oracle_widen.restype = D
             lib.oracle_num_threads.restype = I
+            lib.oracle_set_num_threads.argtypes = [I]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -124,6 +126,11 @@ def _check(rc, name):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls (n < 1: all the host's cores again)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def attn(q, k, v, causal=False, scale=None, kv_len=None):

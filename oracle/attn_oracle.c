@@ -112,6 +112,17 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads of the later calls (for timing the oracle on one core as well as on
+   all of them); n < 1 restores the default.  Touches no arithmetic. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n >= 1 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 /* Is key j visible to query row i of batch b?  Definition of the mask. */
 static int key_valid(long long i, long long j, long long S_q, long long S_kv,
                      int causal, long long kv_len_b)

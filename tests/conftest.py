@@ -8,3 +8,17 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """fp32 parity held to the TF32 bound: how many elements of each case lie
+    beyond the spec pair atol 1e-3 / rtol 1e-2."""
+    try:
+        from gpu_util import TF32_RECORDS
+    except Exception:
+        return
+    if not TF32_RECORDS:
+        return
+    terminalreporter.write_sep("-", "fp32 (TF32) parity: elements beyond atol 1e-3 / rtol 1e-2, all within the TF32 bound")
+    for what, beyond, n, worst in TF32_RECORDS:
+        terminalreporter.write_line(f"{what}: {beyond} of {n} beyond the north-star pair; worst err/bound {worst:.3f}")

@@ -114,10 +114,12 @@ def test_workspace_sizes(lib):
     assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 1, 1, 16, 16, 96, api.LA_BF16) == bad
     assert lib.la_workspace_size(9, 1, 1, 16, 16, 64, api.LA_BF16) == bad
     assert lib.la_workspace_size(api.LA_OP_LAYER_ATTN, 1, 1, 16, 32, 64, api.LA_BF16) == bad
-    # short key ranges never split; half precision needs nothing else
-    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_BF16) == 0
-    # fp32 holds V transposed for the TF32 tensor cores
-    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_F32) == api.fp32_vt_bytes(8, 8, 512, 64)
+    # short key ranges never split; half precision needs only the 256 bytes of
+    # the persistent scheduling's ticket words
+    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_BF16) == 256
+    # fp32 also holds V transposed for the TF32 tensor cores
+    assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 8, 8, 512, 512, 64, api.LA_F32) == \
+        api.fp32_vt_bytes(8, 8, 512, 64) + 256
     assert lib.la_workspace_size(api.LA_OP_QKV_PROJ, 8, 8, 512, 512, 64, api.LA_F32) == 3 * 512 * 512 * 4
     assert lib.la_workspace_size(api.LA_OP_QKV_PROJ, 8, 8, 512, 512, 64, api.LA_BF16) == 0
     # the 100k-token chunked case: partials stay far below the cache itself
@@ -148,7 +150,9 @@ def test_layer_attn_out_checks_workspace_before_launch(lib):
     need = api.workspace_size(api.LA_OP_LAYER_ATTN_OUT, 8, 8, 512, 512, 64, api.torch.float32)
     base = api.workspace_size(api.LA_OP_LAYER_ATTN, 8, 8, 512, 512, 64, api.torch.float32)
     assert need == base + 8 * 512 * 512 * 4 + 512 * 512 * 4     # + merged output + Wo^T
-    def call(ws=FAKE, nb=need - 1, Wo=FAKE):
+    # the last 256 bytes of `need` hold the attention's ticket words, which a
+    # call can do without; one byte short of the rest is refused
+    def call(ws=FAKE, nb=need - 256 - 1, Wo=FAKE):
         return lib.la_layer_attn_out(FAKE, FAKE, None, Wo, None, FAKE, 8, 512, 512, 8, 0, None, api.LA_F32, ws, nb,
                                      None)
     assert call() == api.LA_ERR_WORKSPACE
@@ -181,8 +185,8 @@ def test_layernorm_rejects_bad_arguments(lib):
 def test_layer_attn_ln_checks_arguments_before_launch(lib):
     need = api.workspace_size(api.LA_OP_LAYER_ATTN_LN, 8, 8, 512, 512, 64, api.torch.float32)
     assert need == api.workspace_size(api.LA_OP_LAYER_ATTN_OUT, 8, 8, 512, 512, 64, api.torch.float32) \
-        + 8 * 512 * 512 * 4                                       # + the normalised x
-    def call(g=FAKE, eps=1e-5, Wo=FAKE, bo=None, nb=need - 1):
+        + 8 * 512 * 8                                             # + the row statistics (mean, rstd)
+    def call(g=FAKE, eps=1e-5, Wo=FAKE, bo=None, nb=need - 256 - 1):  # short of all but the ticket words
         return lib.la_layer_attn_ln(FAKE, g, FAKE, eps, FAKE, None, Wo, bo, FAKE, 8, 512, 512, 8, 0, None,
                                     api.LA_F32, FAKE, nb, None)
     assert call() == api.LA_ERR_WORKSPACE

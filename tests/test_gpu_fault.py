@@ -43,18 +43,20 @@ def test_withdrawn_request_does_nothing():
 def test_timeout_in_persistent_form_then_correct_launches():
     """The same on a launch with more work items than SMs (the persistent
     form): every CTA still draws its tickets to the end, so the launches
-    after the timed-out one (which reuse the ticket counter's slots) hand out
-    each item exactly once."""
+    after the timed-out one (reusing the same workspace, hence the same
+    ticket words) hand out each item exactly once."""
     B, H, S, D = 2, 80, 512, 64  # 320 items
     q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=73)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     assert api.get_last_error() == api.LA_OK
+    ws = torch.empty(api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, torch.bfloat16), dtype=torch.uint8,
+                     device="cuda")
     api.debug_inject_timeout(1)
-    api.attn_fwd(qd, kd, vd, causal=True)
+    api.attn_fwd(qd, kd, vd, causal=True, workspace=ws)
     assert api.get_last_error() == api.LA_ERR_TIMEOUT
     want = oracle.attn(q, k, v, causal=True)
-    for i in range(66):  # more launches than counter slots
-        o = api.attn_fwd(qd, kd, vd, causal=True)
+    for i in range(66):
+        o = api.attn_fwd(qd, kd, vd, causal=True, workspace=ws)
         if i in (0, 1, 65):
             assert api.get_last_error() == api.LA_OK
             assert_close(o, want, torch.bfloat16, f"launch {i} after timeout")

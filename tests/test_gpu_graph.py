@@ -41,8 +41,9 @@ def test_graph_replays_persistent_attention_with_new_inputs():
 
 
 def test_graph_replays_interleaved_with_direct_persistent_calls():
-    """Direct persistent launches (taking ticket slots in turn) between
-    replays of a captured one: every launch hands out each item once."""
+    """Direct persistent launches (each with a workspace of its own, under
+    a ticket tag of its own) between replays of a captured one (the same tag
+    on every replay): every launch hands out each item once."""
     B, H, S, D = 4, 40, 512, 128
     dtype = torch.bfloat16
     q, k, v = (t.cuda() for t in inputs.attn_inputs(B, H, S, S, D, dtype, seed=97))

@@ -1,13 +1,15 @@
 """The persistent form of the attention kernel (launches with more work items
 than SMs): items handed out by ticket, barrier phases and the key/value ring
 carried from item to item, inactive items skipped by every role, split
-partials, and the ticket counter's slots reused across many launches.  Each
-case is compared with the fp64 oracle on identical seeded inputs."""
+partials, the ticket words in the workspace reused across many launches, and
+launches on two streams at the same time (each with its own workspace).
+Each case is compared with the fp64 oracle on identical seeded inputs."""
 import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, need_gpu
+import tf32_bound as tb
+from gpu_util import assert_close, assert_within_tf32, need_gpu
 from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
@@ -80,17 +82,73 @@ def test_persistent_with_split_partials():
     assert_close(o_one[r[:, 0], r[:, 1], r[:, 2]], want, dtype, "unsplit")
 
 
-def test_ticket_slots_reused_across_launches():
-    """70 persistent launches (the ticket counter has 64 slots, taken in
-    turn): every launch must hand out each item exactly once."""
+def test_ticket_words_reused_across_launches():
+    """70 persistent launches on one workspace (its ticket words reused, each
+    launch under a tag of its own): every launch must hand out each item
+    exactly once."""
     B, H, S, D = 2, 80, 512, 64
     dtype = torch.bfloat16
     assert _items(B, H, S, dtype, D) > SMS
     q, k, v = inputs.attn_inputs(B, H, S, S, D, dtype, seed=46)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
-    first = api.attn_fwd(qd, kd, vd, causal=True)
-    outs = [api.attn_fwd(qd, kd, vd, causal=True) for _ in range(70)]
+    ws = torch.empty(api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, dtype), dtype=torch.uint8, device="cuda")
+    first = api.attn_fwd(qd, kd, vd, causal=True, workspace=ws)
+    outs = [api.attn_fwd(qd, kd, vd, causal=True, workspace=ws) for _ in range(70)]
     assert api.get_last_error() == api.LA_OK
     for i, o in enumerate(outs):
         assert torch.equal(o, first), f"launch {i}"
     assert_close(first, oracle.attn(q, k, v, causal=True), dtype, "reference launch")
+
+
+def test_fresh_workspace_with_garbage_ticket_words():
+    """A workspace whose first bytes hold leftovers (here: every byte 0xA5,
+    and the tag pattern of other launches) needs no clearing: the launch
+    claims the words under its own tag."""
+    B, H, S, D = 2, 80, 512, 64
+    dtype = torch.bfloat16
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, dtype, seed=47)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    n = api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, dtype)
+    want = oracle.attn(q, k, v, causal=True)
+    for fill in (0xA5, 0x01, 0xFF):
+        ws = torch.full((n,), fill, dtype=torch.uint8, device="cuda")
+        o = api.attn_fwd(qd, kd, vd, causal=True, workspace=ws)
+        assert api.get_last_error() == api.LA_OK
+        assert_close(o, want, dtype, f"workspace filled with {fill:#x}")
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 64)],
+                         ids=lambda p: str(p).replace("torch.", ""))
+def test_two_streams_at_once(dtype, D):
+    """Persistent launches on two streams with no ordering between them, each
+    stream with its own workspace (hence its own ticket words), 24 launches
+    each, interleaved: every output must equal its stream's first and the
+    oracle.  With a ticket counter shared between the streams, items would be
+    taken by the wrong launch and rows left unwritten."""
+    B, H, S = 2, 80, 512
+    assert _items(B, H, S, dtype, D) > SMS
+    ins = [inputs.attn_inputs(B, H, S, S, D, dtype, seed=48 + i) for i in range(2)]
+    dev = [tuple(t.cuda() for t in x) for x in ins]
+    n = api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, dtype)
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    wss = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    outs = [[], []]
+    torch.cuda.synchronize()
+    for it in range(24):
+        for i in range(2):
+            o = torch.full_like(dev[i][0], float("nan"))
+            with torch.cuda.stream(streams[i]):
+                api.attn_fwd(*dev[i], causal=True, out=o, workspace=wss[i], stream=streams[i])
+            outs[i].append(o)
+    torch.cuda.synchronize()
+    assert api.get_last_error() == api.LA_OK
+    for i in range(2):
+        for j, o in enumerate(outs[i]):
+            assert torch.equal(o, outs[i][0]), f"stream {i} launch {j}"
+        want = oracle.attn(*ins[i], causal=True)
+        if dtype == torch.float32:  # early causal rows: the TF32 bound
+            q, k, v = (t.numpy() for t in ins[i])
+            P = oracle.attn_probs(*ins[i][:2], causal=True)
+            assert_within_tf32(outs[i][0], want, tb.attn_bound(q, k, v, P, want, D ** -0.5), f"two streams {i}")
+        else:
+            assert_close(outs[i][0], want, dtype, f"stream {i}")
