@@ -549,6 +549,33 @@ def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
               8, 8, 2048, 64, torch.float32, True, padded=True)
     attn_case("bf16-causal-4096", "bf16 causal B4 H16 S4096 D128", 4, 16, 4096, 128, torch.bfloat16, True)
     attn_case("fp32-small", "fp32 B1 H2 S128 D64 non-causal", 1, 2, 128, 64, torch.float32, False, small=True)
+    if args.only == "attn-window-bf16":
+        # one window of the chunked mode on its own (profiling: 0.4 GB on the
+        # device instead of the whole 100k-token run): 4096 queries against
+        # 40960 keys, causal rows aligned to the end
+        B, H, S_q, S_kv, D = 2, 16, 4096, 40960, 64
+        q, k, v = (t.to(dev) for t in inputs.attn_inputs(B, H, S_q, S_kv, D, torch.bfloat16, seed=0))
+        o = torch.empty_like(q)
+        n = api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S_q, S_kv, D, torch.bfloat16)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+        ms = _time_steps(lambda: api.attn_fwd(q, k, v, causal=True, out=o, workspace=ws, stream=stream),
+                         Kx, 3, flush, stream, barrier) / Kx
+        fl = flops.attn_flops(B, H, S_q, S_kv, D, True)
+        res["bf16 causal window B2 H16 S_q4096 S_kv40960 D64"] = {
+            "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2), "gflop": round(fl / 1e9, 1)}
+        return res
+    if args.only == "sublayer-fp32":
+        # the headline step alone (profiling)
+        B, S, dm, H = HEADLINE["B"], HEADLINE["S"], HEADLINE["d_model"], HEADLINE["H"]
+        x, Wq, bq = (t.to(dev) for t in inputs.layer_inputs(B, S, dm, torch.float32, seed=0))
+        y = torch.empty_like(x)
+        ws = torch.empty(api.workspace_size(api.LA_OP_LAYER_ATTN, B, H, S, S, dm // H, torch.float32),
+                         dtype=torch.uint8, device=dev)
+        ms = _time_steps(lambda: api.layer_attn(x, Wq, bq, H, out=y, workspace=ws, stream=stream),
+                         Kx, 3, flush, stream, barrier) / Kx
+        fl = flops.proj_flops(B, S, dm) + flops.attn_flops(B, H, S, S, dm // H, False)
+        res[HEADLINE_NAME] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2)}
+        return res
 
     def layer_out_case(key, name, dt):
         """The sublayer (la_layer_attn), the sublayer with its output projection
@@ -844,7 +871,7 @@ def main():
                                                   "(JSON lines)")
     ap.add_argument("--only", choices=["fp32-causal-2048", "fp32-causal-2048-padded", "bf16-causal-4096",
                                        "fp32-small", "small-graph", "layer-out-fp32", "layer-out-bf16", "layer-out-f16",
-                                       "chunked-100k"],
+                                       "chunked-100k", "attn-window-bf16", "sublayer-fp32"],
                     help="time one named attention workload alone and print its figures (no contract line)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

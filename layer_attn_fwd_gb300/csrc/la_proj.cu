@@ -123,12 +123,11 @@ __device__ __forceinline__ uint4 pack_unit(const float* v, int u) {
 // the kind::tf32 product reads only the top 19 bits; the copy into shared
 // memory left x unrounded).
 template <typename T>
-__device__ __forceinline__ uint4 ln_unit(uint4 w, const T* gamma, const T* beta, int col, float mu, float rs);
+__device__ __forceinline__ uint4 ln_unit(uint4 w, uint4 gw, uint4 bw, float mu, float rs);
 template <>
-__device__ __forceinline__ uint4 ln_unit<float>(uint4 w, const float* gamma, const float* beta, int col, float mu,
-                                                float rs) {
-  const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + col));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(beta + col));
+__device__ __forceinline__ uint4 ln_unit<float>(uint4 w, uint4 gw, uint4 bw, float mu, float rs) {
+  const float4 g = make_float4(__uint_as_float(gw.x), __uint_as_float(gw.y), __uint_as_float(gw.z), __uint_as_float(gw.w));
+  const float4 b = make_float4(__uint_as_float(bw.x), __uint_as_float(bw.y), __uint_as_float(bw.z), __uint_as_float(bw.w));
   uint4 o;
   o.x = __float_as_uint(fmaf((__uint_as_float(w.x) - mu) * rs, g.x, b.x)) + 0x1000u;
   o.y = __float_as_uint(fmaf((__uint_as_float(w.y) - mu) * rs, g.y, b.y)) + 0x1000u;
@@ -137,9 +136,7 @@ __device__ __forceinline__ uint4 ln_unit<float>(uint4 w, const float* gamma, con
   return o;
 }
 template <typename T>
-__device__ __forceinline__ uint4 ln_unit_half(uint4 w, const T* gamma, const T* beta, int col, float mu, float rs) {
-  const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gamma + col));
-  const uint4 bw = __ldg(reinterpret_cast<const uint4*>(beta + col));
+__device__ __forceinline__ uint4 ln_unit_half(uint4 w, uint4 gw, uint4 bw, float mu, float rs) {
   const uint32_t xs[4] = {w.x, w.y, w.z, w.w}, gs[4] = {gw.x, gw.y, gw.z, gw.w}, bs[4] = {bw.x, bw.y, bw.z, bw.w};
   uint32_t o[4];
 #pragma unroll
@@ -155,14 +152,12 @@ __device__ __forceinline__ uint4 ln_unit_half(uint4 w, const T* gamma, const T* 
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 template <>
-__device__ __forceinline__ uint4 ln_unit<__nv_bfloat16>(uint4 w, const __nv_bfloat16* gamma,
-                                                        const __nv_bfloat16* beta, int col, float mu, float rs) {
-  return ln_unit_half<__nv_bfloat16>(w, gamma, beta, col, mu, rs);
+__device__ __forceinline__ uint4 ln_unit<__nv_bfloat16>(uint4 w, uint4 gw, uint4 bw, float mu, float rs) {
+  return ln_unit_half<__nv_bfloat16>(w, gw, bw, mu, rs);
 }
 template <>
-__device__ __forceinline__ uint4 ln_unit<__half>(uint4 w, const __half* gamma, const __half* beta, int col, float mu,
-                                                 float rs) {
-  return ln_unit_half<__half>(w, gamma, beta, col, mu, rs);
+__device__ __forceinline__ uint4 ln_unit<__half>(uint4 w, uint4 gw, uint4 bw, float mu, float rs) {
+  return ln_unit_half<__half>(w, gw, bw, mu, rs);
 }
 
 template <typename T, int BNP, int NSP, bool LN>
@@ -331,6 +326,12 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP, LN>::THREADS, 1)
       }
       for (int kt = 0; kt < n_k; ++kt, ++it) {
         const int s = it % NSP, r = it / NSP;
+        uint4 gv[8], bv[8];  // this stage's gamma and beta, requested before the wait for the stage
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          gv[u] = __ldg(reinterpret_cast<const uint4*>(gamma + kt * CW + u * (CW / 8)));
+          bv[u] = __ldg(reinterpret_cast<const uint4*>(beta + kt * CW + u * (CW / 8)));
+        }
         if (!__all_sync(0xffffffffu, mbar_wait(&full[s], r & 1, ab, SITE_PROJ_FULL))) { ok = false; break; }
         const uint32_t line = smem_u32(smem + C::OFF_A + s * C::A_STAGE) + xr * 128;
         // all eight loads first, then the arithmetic, then the stores (the
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(PCfg<T, BNP, NSP, LN>::THREADS, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u) xv[u] = lds128(line + ((u ^ (xr & 7)) << 4));
 #pragma unroll
-        for (int u = 0; u < 8; ++u) xv[u] = ln_unit<T>(xv[u], gamma, beta, kt * CW + u * (CW / 8), mu, rs);
+        for (int u = 0; u < 8; ++u) xv[u] = ln_unit<T>(xv[u], gv[u], bv[u], mu, rs);
 #pragma unroll
         for (int u = 0; u < 8; ++u) sts128(line + ((u ^ (xr & 7)) << 4), xv[u]);
         fence_proxy_async_smem();  // the tensor cores read the stage through the async proxy

@@ -56,6 +56,18 @@ def test_noalloc_matches_workspace_entry(case):
         assert_close(o, ref.double().cpu().numpy(), dt, f"call {call + 1}")
 
 
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16], ids=lambda d: str(d).split(".")[-1])
+def test_noalloc_without_keys_writes_zero_rows(dt):
+    """S_kv = 0: every row is a zero row, for fp32 as well (no V to transpose)."""
+    lib = api.load()
+    q = torch.randn(1, 2, 40, 64, device="cuda").to(dt)
+    kv = torch.empty(1, 2, 0, 64, device="cuda", dtype=dt)
+    o = torch.full_like(q, float("nan"))
+    assert _noalloc(lib, q, kv, kv, o, False, api._DT[dt]) == api.LA_OK
+    assert api.get_last_error() == api.LA_OK
+    assert torch.count_nonzero(o).item() == 0
+
+
 def test_noalloc_refuses_scratch_beyond_its_array():
     lib = api.load()
     # fp32 with V transposed needs 8*8*64*2048*4 = 32 MiB > 16 MiB: refused before any launch
