@@ -509,8 +509,21 @@ def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
     def wanted(key):
         return not args.only or args.only == key
 
+    def fits(name, nbytes):
+        """Memory pre-check: a workload whose device tensors would not fit in
+        the free device memory is recorded as skipped, with the reason,
+        instead of being run."""
+        free = torch.cuda.mem_get_info(dev)[0]
+        if nbytes * 1.1 + (256 << 20) > free:
+            res[name] = {"skipped": f"needs about {nbytes / 1e9:.2f} GB on the device, {free / 1e9:.2f} GB free"}
+            return False
+        return True
+
     def attn_case(key, name, B, H, S, D, dt, causal, padded=False, small=False):
         if not wanted(key):
+            return
+        esz = torch.tensor([], dtype=dt).element_size()
+        if not fits(name, 4 * B * H * S * D * esz + api.workspace_size(api.LA_OP_ATTN_FWD, B, H, S, S, D, dt)):
             return
         qh, kh, vh = inputs.attn_inputs(B, H, S, S, D, dt, seed=0)
         q, k, v = (t.to(dev) for t in (qh, kh, vh))
@@ -584,6 +597,10 @@ def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
         if not wanted(key):
             return
         B, S, dm, H = 8, 512, 512, 8
+        esz = torch.tensor([], dtype=dt).element_size()
+        if not fits(name, (4 * B * S * dm + 6 * dm * dm) * esz
+                    + api.workspace_size(api.LA_OP_LAYER_ATTN_LN, B, H, S, S, dm // H, dt)):
+            return
         x, Wq, bq = (t.to(dev) for t in inputs.layer_inputs(B, S, dm, dt, seed=0))
         Wo, bo = (t.to(dev) for t in inputs.out_proj_inputs(dm, dt, seed=1))
         y = torch.empty_like(x)
@@ -683,6 +700,11 @@ def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
 
     # chunked 100k-token mode: 25 windows of 4096 (the last 1696) per step
     B, H, S, D, C = 2, 16, 100000, 64, 4096
+    name_c = f"chunked bf16 causal B{B} H{H} S{S} D{D}, windows of {C}"
+    # windowed q, k, v and outputs, the cache's K and V
+    if not fits(name_c, 6 * B * H * S * D * 2 + api.workspace_size(api.LA_OP_ATTN_CHUNKED, B, H, C, S, D,
+                                                                   torch.bfloat16)):
+        return res
     q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=0)
     wins = inputs.chunk_bounds(S, C)
     qs = [q[:, :, s:s + L].contiguous().to(dev) for s, L in wins]
@@ -731,7 +753,7 @@ def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
                                        f"pairs, fp64, OpenMP); extrapolated per pair to the whole workload "
                                        f"({t_full / 3600:.1f} h)"}
         del q, k, v
-    res["chunked bf16 causal B2 H16 S100000 D64, windows of 4096"] = r
+    res[name_c] = r
     st = api.get_last_error(stream)
     if st != api.LA_OK:
         raise RuntimeError(f"device status after the extra workloads: {api.status_string(st)}")
@@ -873,7 +895,16 @@ def main():
                                        "fp32-small", "small-graph", "layer-out-fp32", "layer-out-bf16", "layer-out-f16",
                                        "chunked-100k", "attn-window-bf16", "sublayer-fp32"],
                     help="time one named attention workload alone and print its figures (no contract line)")
+    ap.add_argument("--require-clean", action="store_true",
+                    help="refuse to run unless the git work tree matches its commit (tracked files unmodified), "
+                         "so that a logged number names the code it measured")
     args = ap.parse_args()
+    if args.require_clean:
+        c = _commit()
+        if c is None or c.endswith("+dirty"):
+            print(json.dumps({"error": "--require-clean: " + ("not a git work tree" if c is None
+                                                              else f"tracked files differ from {c[:-6]}")}))
+            sys.exit(2)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
