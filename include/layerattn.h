@@ -80,9 +80,13 @@ typedef enum {
 
 /*
  * Growing key/value cache for the chunked mode.  k and v are caller-owned
- * device buffers [B, H, S_max, D] of element type `dtype`; positions
- * [0, len) hold valid keys/values.  la_attn_chunked() appends to it and
- * advances `len` on the host struct.
+ * device buffers of element type `dtype`: k [B, H, S_max, D]; v the same
+ * for bf16/fp16, and for fp32 V transposed, [B, H, D, S_max] (the TF32
+ * tensor cores take the PV product's V only with keys contiguous, so each
+ * window's values are appended transposed once instead of the whole cache
+ * being transposed on every window; fp32 S_max must then be a multiple of
+ * 4).  Positions [0, len) hold valid keys/values.  la_attn_chunked()
+ * appends to it and advances `len` on the host struct.
  */
 typedef struct {
     void *k;
@@ -159,9 +163,10 @@ la_status la_attn_fwd(const void *q, const void *k, const void *v, void *o,
  * cache->len grows by chunk.  Calling it window after window over a sequence
  * gives the same result as attending the whole sequence at once.
  * cache->len + chunk must not exceed cache->S_max; cache->dtype, B, H and D
- * describe all five tensors.  ws: as for la_attn_fwd (fp32 transposes the
- * cache's valid V rows into it on every call), sized with
- * la_workspace_size(LA_OP_ATTN_CHUNKED, B, H, chunk, S_max, D, dtype).
+ * describe all five tensors; an fp32 cache whose S_max is not a multiple of
+ * 4 is refused (LA_ERR_INVALID).  ws: as for la_attn_fwd, sized with
+ * la_workspace_size(LA_OP_ATTN_CHUNKED, B, H, chunk, S_max, D, dtype) (no
+ * V^T scratch: an fp32 cache already holds V transposed).
  * On any non-OK status cache->len is unchanged.
  */
 la_status la_attn_chunked(const void *q_chunk, const void *k_chunk, const void *v_chunk,

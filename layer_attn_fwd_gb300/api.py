@@ -249,11 +249,18 @@ def attn_fwd_noalloc(q, k, v, causal=False, scale=None, kv_len=None, out=None, s
 
 
 class KVCache:
-    """Caller-owned growing key/value cache [B,H,S_max,D] for the chunked mode."""
+    """Caller-owned growing key/value cache for the chunked mode: k
+    [B,H,S_max,D]; v the same for bf16/fp16 and transposed, [B,H,D,S_max],
+    for fp32 (S_max then rounded up to a multiple of 4)."""
 
     def __init__(self, B, H, S_max, D, dtype, device="cuda"):
+        if dtype == torch.float32:
+            S_max = (S_max + 3) // 4 * 4
         self.k = torch.empty(B, H, S_max, D, dtype=dtype, device=device)
-        self.v = torch.empty(B, H, S_max, D, dtype=dtype, device=device)
+        if dtype == torch.float32:
+            self.v = torch.empty(B, H, D, S_max, dtype=dtype, device=device)
+        else:
+            self.v = torch.empty(B, H, S_max, D, dtype=dtype, device=device)
         self.c = la_kv_cache(self.k.data_ptr(), self.v.data_ptr(), B, H, D, S_max, 0, _DT[dtype])
 
     @property

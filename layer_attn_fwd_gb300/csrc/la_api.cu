@@ -689,15 +689,27 @@ la_status la_attn_chunked(const void* q_chunk, const void* k_chunk, const void* 
       !aligned16(cache->k) || !aligned16(cache->v))
     return LA_ERR_INVALID;
   if (ws != nullptr && !aligned16(ws)) return LA_ERR_INVALID;
-  if (chunk == 0) return LA_OK;
   const la_dtype dt = cache->dtype;
+  // fp32: the cache holds V^T [B, H, D, S_max]; its rows must start 16-byte
+  // aligned for the tensor map
+  if (dt == LA_F32 && cache->S_max % 4 != 0) return LA_ERR_INVALID;
+  if (chunk == 0) return LA_OK;
   const int S_kv = cache->len + chunk;
-  if ((ws == nullptr ? 0 : ws_bytes) < vt_bytes(dt, B, H, S_kv, D)) return LA_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(st);
-  if (launch_kv_append(k_chunk, v_chunk, cache->k, cache->v, B, H, chunk, D, cache->S_max, cache->len,
-                       elem_bytes(dt), cs) != cudaSuccess)
+  if (dt == LA_F32) {
+    // keys appended as rows; values appended transposed, at columns
+    // [len, len + chunk) of every (b, h) block of V^T
+    if (launch_kv_append(k_chunk, nullptr, cache->k, nullptr, B, H, chunk, D, cache->S_max, cache->len,
+                         elem_bytes(dt), cs) != cudaSuccess ||
+        launch_transpose32(v_chunk, static_cast<long long>(chunk) * D,
+                           static_cast<float*>(cache->v) + cache->len, cache->S_max,
+                           static_cast<long long>(B) * H, chunk, D, cs) != cudaSuccess)
+      return LA_ERR_CUDA;
+  } else if (launch_kv_append(k_chunk, v_chunk, cache->k, cache->v, B, H, chunk, D, cache->S_max, cache->len,
+                              elem_bytes(dt), cs) != cudaSuccess) {
     return LA_ERR_CUDA;
-  const KVView kv{cache->k, cache->v, cache->S_max, nullptr, 0};
+  }
+  const KVView kv{cache->k, cache->v, cache->S_max, dt == LA_F32 ? cache->v : nullptr, cache->S_max};
   s = run_attention(q_chunk, kv, o_chunk, static_cast<long long>(H) * chunk * D, static_cast<long long>(chunk) * D,
                     D, B, H, chunk, S_kv, D, causal, scale, nullptr, dt, ws, ws_bytes, cs);
   if (s == LA_OK) cache->len = S_kv;
@@ -805,8 +817,9 @@ size_t la_workspace_size(int op, int B, int H, int S_q, int S_kv, int D, la_dtyp
   if (check_attn_args(B, H, S_q, S_kv, D, 1.f, dt) != LA_OK) return bad;
   switch (op) {
     case LA_OP_ATTN_FWD:
-    case LA_OP_ATTN_CHUNKED:
       return attn_ws_bytes(dt, B, H, S_q, S_kv, D, true);
+    case LA_OP_ATTN_CHUNKED:  // (an fp32 cache holds V^T already)
+      return attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);
     case LA_OP_LAYER_ATTN: {
       if (S_q != S_kv) return bad;
       return layer_fixed_bytes(B, S_q, H * D, H, dt) + attn_ws_bytes(dt, B, H, S_q, S_kv, D, false);

@@ -126,7 +126,8 @@ cudaError_t launch_transpose32(const void* src, long long src_batch, void* dst, 
 cudaError_t launch_layernorm(la_dtype dt, const void* x, const void* gamma, const void* beta, void* y, long long M,
                              int d, float eps, cudaStream_t st, bool pdl = false, float2* stats = nullptr);
 
-// Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`.
+// Copy k_src, v_src [B,H,rows,D] into k_dst, v_dst [B,H,S_max,D] at row `at`
+// (keys only when v_src is null).
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
                              int rows, int D, int S_max, int at, int elem_bytes, cudaStream_t st);
 

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   }
 }
 
-// blockIdx.y selects k (0) or v (1).
+// blockIdx.y selects k (0) or v (1); a keys-only launch has one row of blocks.
 __global__ void __launch_bounds__(256)
     kv_append_kernel(const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint8_t* k_dst,
                      uint8_t* v_dst, long long n_vec, int vec_per_row, int rows, long long dst_head_bytes,
@@ -411,7 +411,7 @@ cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, 
   if (n_vec == 0) return cudaSuccess;
   const long long want = (n_vec + 255) / 256;
   const int cap = sm_count() * 4;
-  dim3 grid(static_cast<unsigned>(want < cap ? want : cap), 2);
+  dim3 grid(static_cast<unsigned>(want < cap ? want : cap), v_src != nullptr ? 2 : 1);  // keys only without v
   const long long row_bytes = static_cast<long long>(D) * elem_bytes;
   return launch("kv_append_kernel", kv_append_kernel, grid, dim3(256), 0, st, false,
                 reinterpret_cast<const uint4*>(k_src), reinterpret_cast<const uint4*>(v_src),

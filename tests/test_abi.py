@@ -109,6 +109,16 @@ def test_chunked_rejects_overflowing_cache_and_keeps_len(lib):
     assert c.len == 90
 
 
+def test_chunked_fp32_cache_needs_s_max_multiple_of_4(lib):
+    """An fp32 cache keeps V transposed, rows S_max long: S_max must keep
+    each row 16-byte aligned; the refusal comes before any launch and leaves
+    len unchanged."""
+    c = api.la_kv_cache(0x7f0000000000, 0x7f0000100000, 2, 16, 64, 102, 40, api.LA_F32)
+    st = lib.la_attn_chunked(FAKE, FAKE, FAKE, ctypes.byref(c), FAKE, 8, 1, 0.125, None, 0, None)
+    assert st == api.LA_ERR_INVALID
+    assert c.len == 40
+
+
 def test_workspace_sizes(lib):
     bad = ctypes.c_size_t(-1).value
     assert lib.la_workspace_size(api.LA_OP_ATTN_FWD, 1, 1, 16, 16, 96, api.LA_BF16) == bad
@@ -122,6 +132,8 @@ def test_workspace_sizes(lib):
         api.fp32_vt_bytes(8, 8, 512, 64) + 256
     assert lib.la_workspace_size(api.LA_OP_QKV_PROJ, 8, 8, 512, 512, 64, api.LA_F32) == 3 * 512 * 512 * 4
     assert lib.la_workspace_size(api.LA_OP_QKV_PROJ, 8, 8, 512, 512, 64, api.LA_BF16) == 0
+    # the chunked mode needs no V^T scratch: an fp32 cache holds V transposed
+    assert lib.la_workspace_size(api.LA_OP_ATTN_CHUNKED, 8, 8, 512, 512, 64, api.LA_F32) == 256
     # the 100k-token chunked case: partials stay far below the cache itself
     n = lib.la_workspace_size(api.LA_OP_ATTN_CHUNKED, 2, 16, 4096, 100000, 64, api.LA_BF16)
     assert n != bad and n < 2 * 16 * 100000 * 64 * 2 * 4

@@ -50,6 +50,27 @@ def test_chunked_small(dtype, D):
     assert_close(o, oracle.attn_chunked(q, k, v, C), dtype, "chunked oracle")
 
 
+def test_chunked_fp32_cache_holds_v_transposed():
+    """fp32: each window's values are appended to the cache transposed (V^T
+    [B, H, D, S_max]), including windows that start off a 16-byte boundary
+    (250-row windows), and the attention reads them from there: the cache
+    equals V^T bit for bit and the output matches the oracle."""
+    B, H, S, D, C = 2, 3, 1000, 64, 250
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=53)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    cache = api.KVCache(B, H, S + 3, D, torch.float32)
+    assert cache.c.S_max == 1004 and tuple(cache.v.shape) == (B, H, D, 1004)
+    outs = []
+    for s0, L in inputs.chunk_bounds(S, C):
+        sl = slice(s0, s0 + L)
+        outs.append(api.attn_chunked(qd[:, :, sl].contiguous(), kd[:, :, sl].contiguous(),
+                                     vd[:, :, sl].contiguous(), cache, causal=True))
+    assert api.get_last_error() == api.LA_OK
+    assert torch.equal(cache.v[:, :, :, :S].cpu(), v.transpose(2, 3))
+    assert torch.equal(cache.k[:, :, :S].cpu(), k)
+    assert_close(torch.cat(outs, dim=2), oracle.attn(q, k, v, causal=True), torch.float32, "fp32 chunked, V^T cache")
+
+
 def test_chunk_of_one_row():
     q, k, v = inputs.attn_inputs(1, 2, 40, 40, 64, torch.bfloat16, seed=52)
     o = _run_chunked(q.cuda(), k.cuda(), v.cuda(), 1)
