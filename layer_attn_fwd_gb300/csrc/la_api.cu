@@ -252,7 +252,12 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
   size_t w_left = ws == nullptr ? 0 : ws_bytes;
   const void* vt = kv.vt;
   long long vt_ld = kv.vt_ld;
-  if (dt == LA_F32 && vt == nullptr) {
+  // fp32 with a single key tile and one CTA per item (the small shapes): the
+  // attention kernel transposes its one V tile in shared memory itself, so
+  // there is no V^T pre-pass launch and no V^T workspace
+  const long long items1 = static_cast<long long>((S_q + sh.rows_per_cta - 1) / sh.rows_per_cta) * B * H;
+  const bool v_raw = dt == LA_F32 && vt == nullptr && S_kv <= sh.block_n && items1 <= device_sms();
+  if (dt == LA_F32 && vt == nullptr && !v_raw) {
     const size_t need = vt_bytes(dt, B, H, S_kv, D);
     if (w_left < need) return LA_ERR_WORKSPACE;
     vt_ld = vt_pad(S_kv);
@@ -280,7 +285,7 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
   s = map_bhsd(&tk, kv.k, dt, B, H, S_kv, D, D, kv.rows_alloc * D, static_cast<long long>(H) * kv.rows_alloc * D,
                sh.box_kv_rows, sh.box_cols);
   if (s != LA_OK) return s;
-  if (dt == LA_F32) {
+  if (dt == LA_F32 && !v_raw) {
     // V^T: keys innermost (the K dimension of the PV product), head dims as rows
     s = map_4d(&tv, vt, dt, S_kv, D, H, B, vt_ld, static_cast<long long>(D) * vt_ld,
                static_cast<long long>(H) * D * vt_ld, sh.box_cols, D);
@@ -309,6 +314,7 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
   a.sched = sched;
   a.sched_gen = next_sched_tag();
   a.skip_loads = g_skip_loads_once.exchange(0);
+  a.v_raw = v_raw ? 1 : 0;
 #if LA_CHECKED
   // extents for the bounds checks: [B, H, S_q, D] elements either layout
   a.o_elems = static_cast<long long>(B) * H * S_q * D;

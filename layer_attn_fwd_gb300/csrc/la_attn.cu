@@ -306,6 +306,13 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using C = Cfg<T, D, NQ, BN, NS, SP, PERS>;
   constexpr bool TF32 = Elem<T>::tf32;
+  // fp32 items of one key tile, one per CTA (a.v_raw): V arrives row-major in
+  // the second stage's value buffer, unused with one key tile, and the TMA
+  // warp transposes it into the first stage's V^T tile (v_full[1]: the raw
+  // tile landed; v_full[0]: V^T written; both unused when keys and values
+  // share k_full)
+  constexpr bool VRAW_OK = C::VT && C::KVM && !PERS && NS >= 2;
+  const bool vraw = VRAW_OK && a.v_raw != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
         for (int j = w.jb; j < w.je_all; ++j, ++it) {
           const int s = it % NS, r = it / NS;
           if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, ab, SITE_K_EMPTY)) { ok = false; break; }
-          mbar_arrive_expect_tx(&k_full[s], C::KVM ? 2 * C::KV_TILE : C::KV_TILE);
+          mbar_arrive_expect_tx(&k_full[s], (C::KVM && !vraw) ? 2 * C::KV_TILE : C::KV_TILE);
           for (int c = 0; c < C::NCH; ++c)
             tma_load_4d(&tm_k, &k_full[s], smem + C::OFF_K + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW,
                         j * BN, w.h, w.b, pol_kv);
@@ -498,9 +505,17 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
             mbar_arrive_expect_tx(vbar, C::KV_TILE);
           }
           if constexpr (C::VT) {
-            for (int c = 0; c < BN / C::CW; ++c)
-              tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW, 0,
-                          w.h, w.b, pol_kv);
+            if (vraw) {  // the item's one value tile, row-major, into the second stage's buffer
+              mbar_arrive_expect_tx(&v_full[1], C::KV_TILE);
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_4d(&tm_v, &v_full[1], smem + C::OFF_V + C::KV_TILE + c * C::KV_CHUNK, c * C::CW, j * BN,
+                            w.h, w.b, pol_kv);
+              last_v[1] = 0;
+            } else {
+              for (int c = 0; c < BN / C::CW; ++c)
+                tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::VT_CHUNK, j * BN + c * C::CW,
+                            0, w.h, w.b, pol_kv);
+            }
           } else {
             for (int c = 0; c < C::NCH; ++c)
               tma_load_4d(&tm_v, vbar, smem + C::OFF_V + s * C::KV_TILE + c * C::KV_CHUNK, c * C::CW, j * BN,
@@ -533,6 +548,41 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
       }
     }
     __syncwarp();
+    if constexpr (VRAW_OK) {
+      // V [keys, D] (128-byte rows of CW head dims, chunk c = dims c*CW..) into
+      // V^T [D, keys] (128-byte rows of CW keys, chunk jc = keys jc*CW..), both
+      // in the 128-byte swizzle the tensor copies use (16-byte unit u of row r
+      // at u ^ r%8), by 4x4 blocks: four 16-byte loads, four 16-byte stores
+      if (vraw && __shfl_sync(0xffffffffu, last_v[1], 0) == 0 &&
+          __all_sync(0xffffffffu, mbar_wait(&v_full[1], 0, ab, SITE_V_FULL))) {
+        const uint32_t src = smem_u32(smem + C::OFF_V + C::KV_TILE);
+        const uint32_t dst = smem_u32(smem + C::OFF_V);
+        constexpr int DB = D / 4;  // 4x4 blocks across the head dims
+#pragma unroll 1
+        for (int blk = lane; blk < (BN / 4) * DB; blk += 32) {
+          const int k0 = 4 * (blk / DB), d0 = 4 * (blk % DB);
+          const int c = d0 / C::CW, u = (d0 % C::CW) / 4;
+          uint32_t e[4][4];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int r = k0 + rr;
+            const uint4 x = lds128(src + c * C::KV_CHUNK + r * 128 + ((u ^ (r & 7)) << 4));
+            e[rr][0] = x.x, e[rr][1] = x.y, e[rr][2] = x.z, e[rr][3] = x.w;
+          }
+          const int jc = k0 / C::CW, u2 = (k0 % C::CW) / 4;
+#pragma unroll
+          for (int dd = 0; dd < 4; ++dd) {
+            const int d = d0 + dd;
+            sts128(dst + jc * C::VT_CHUNK + d * 128 + ((u2 ^ (d & 7)) << 4),
+                   make_uint4(e[0][dd], e[1][dd], e[2][dd], e[3][dd]));
+          }
+        }
+        fence_proxy_async_smem();  // the PV products read the tile through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&v_full[0]);
+      }
+      __syncwarp();
+    }
     __syncthreads();  // teardown rendezvous
     if (lane == 0 && *abort_flag) {
       // let the copies still in flight land before the CTA's shared memory goes away
@@ -626,7 +676,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
           const int sn = (i + 1) % NS, rn = (i + 1) / NS;
           const uint64_t bV = dV + ((s * C::KV_TILE) >> 4);
           const uint64_t bK = dK + ((sn * C::KV_TILE) >> 4);
-          bool v_ready = C::KVM, k_next = false;
+          bool v_ready = C::KVM && !vraw, k_next = false;
 #pragma unroll
           for (int tt = 0; tt < TPW; ++tt) {
             const int t = m + tt * C::MW;

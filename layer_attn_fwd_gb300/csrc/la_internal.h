@@ -73,6 +73,7 @@ struct AttnArgs {
   unsigned sched_gen;         // this launch's tag in the high half of both words (never 0)
   uint32_t* err;              // device error word
   int skip_loads;             // test hook: issue no TMA load, so every wait runs out
+  int v_raw;                  // fp32, one key tile, one CTA per item: tm_v maps V itself and the kernel transposes it
 #if LA_CHECKED
   long long o_elems;          // elements of the output buffer
   long long part_elems;       // elements of part_o (part_lse holds part_elems / D)

@@ -220,3 +220,23 @@ def test_workload_bf16_causal_4096(seed):
     rows = inputs.sample_rows(B, H, S, n=256, seed=32 + 100 * seed, forced=(0, 255, 256, 4095))
     want = oracle.attn_rows(q, k, v, rows, causal=True)
     assert_close(_sampled(o, rows), want, torch.bfloat16, f"bf16 causal 4096, seed {seed}")
+
+
+@pytest.mark.parametrize("D,S_q,S_kv", [(64, 128, 128), (64, 200, 100), (64, 77, 1), (128, 64, 64), (128, 100, 37)])
+def test_fp32_one_key_tile_transposes_v_in_kernel(D, S_q, S_kv):
+    """fp32 calls of one key tile and one CTA per item transpose V inside
+    the attention kernel (no V^T pre-pass): bit for bit what the pre-pass
+    path computes (the same inputs as one call of more items than SMs, which
+    takes the persistent form and the pre-pass), and within the TF32 bound
+    of the oracle.  Ragged key counts leave zero-filled rows in the tile."""
+    B, H = 2, 80
+    q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, torch.float32, seed=131 + D + S_kv)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    whole = api.attn_fwd(qd, kd, vd, causal=True)  # 160 items or more: persistent form, V^T pre-pass
+    halves = torch.cat([api.attn_fwd(qd[b:b + 1], kd[b:b + 1], vd[b:b + 1], causal=True) for b in range(B)])
+    assert api.get_last_error() == api.LA_OK
+    assert torch.equal(whole, halves)
+    want = oracle.attn(q, k, v, causal=True)
+    P = oracle.attn_probs(q, k, causal=True)
+    assert_within_tf32(halves, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5),
+                       f"in-kernel V transpose D={D} S_kv={S_kv}")
