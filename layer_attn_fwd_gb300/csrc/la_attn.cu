@@ -89,7 +89,7 @@ constexpr int pow2_at_least(int x) {
 // PERS: the persistent form, for launches with more work items than SMs;
 // otherwise each CTA runs exactly one item (no item hand-off, and the
 // epilogue stages its stores in the dead Q tiles).
-template <typename T, int D_, int NQ_, int BN_, int NS_, bool SP_, bool PERS = true>
+template <typename T, int D_, int NQ_, int BN_, int NS_, bool PERS = true>
 struct Cfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, NS = NS_;
   static constexpr int E = sizeof(T);
@@ -102,29 +102,20 @@ struct Cfg {
   // Q as the A operand of QK^T from tensor memory when it fits: the product
   // then reads only K from shared memory (half the operand traffic).
   static constexpr int QCOLS = D * E / 4;                  // 32-bit TMEM columns of one Q row
-  // SP: P gets tensor-memory columns of its own instead of overwriting S,
-  // so that QK^T of the next key tile runs while the softmax of this one
-  // works (chosen per configuration: it pays where the tile's MMAs, not its
-  // softmax, are the longer part).  Without Q in tensor memory Q stays in
-  // shared memory, double buffered so the next item's Q loads meanwhile.
-  static constexpr bool SP = SP_;
-  static constexpr int P_COLS = SP ? BN * E / 4 : 0;       // 32-bit TMEM columns of P (SP)
-  static constexpr bool QT = NQ * (BN + P_COLS + D + QCOLS) <= 512;
-  static constexpr int QB = (SP && !QT) ? 2 : 1;           // Q buffers in shared memory
+  static constexpr bool QT = NQ * (BN + D + QCOLS) <= 512;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QB * NQ * Q_TILE;
+  static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + NS * KV_TILE;
   static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp (PERS)
   static constexpr int OFF_BAR = OFF_STG + (PERS ? NQ * 4 * 4096 : 0);
-  // q_full[QB], q_empty[QB], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ],
-  // o_full[NQ], o_free[NQ], mma_done, qt_full, item_full[NR], item_empty[NR], s_free[NQ], pv_done[NQ]
+  // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ],
+  // o_full[NQ], o_free[NQ], mma_done, qt_full, item_full[NR], item_empty[NR]
   static constexpr int NR = 4;  // work items handed from the scheduling thread to the other roles
-  static constexpr int NBAR = 2 * QB + 4 * NS + 4 * NQ + 2 + 2 * NR + 2 * NQ;
+  static constexpr int NBAR = 2 + 4 * NS + 4 * NQ + 2 + 2 * NR;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, then the item ring
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 4 * NR + 1024;  // + slack for 1024-byte alignment
-  // per query tile: S (P over it, or P after it with SP), O, then Q (QT)
-  static constexpr int P_COL = SP ? BN : 0;
-  static constexpr int O_COL = BN + P_COLS;
+  // per query tile: S (P over it), O, then Q (QT)
+  static constexpr int O_COL = BN;
   static constexpr int TILE_COLS = O_COL + D + (QT ? QCOLS : 0);
   static constexpr int TMEM_COLS = pow2_at_least(NQ * TILE_COLS);
   static constexpr int QK_STEPS = D * E / 32;              // one MMA consumes 32 bytes of a row
@@ -139,11 +130,11 @@ struct Cfg {
   // (measured: fp32 D=64 +5%, bf16 D=64 +3%).  With Q in shared memory one
   // warp, which keeps the strict PV_0, S_0, PV_1, S_1 order (measured: two
   // warps cost bf16 D=128 10%).
-  static constexpr int MW = (QT || SP) ? NQ : 1;
+  static constexpr int MW = QT ? NQ : 1;
   // One barrier pair per key/value stage (KVM) where measured faster: with Q
   // in tensor memory (fp32 D=64 +3%, bf16 D=64 +7%); bf16 D=128 with its
   // two 64 KB stages needs the key slot back before PV is done (-7%).
-  static constexpr bool KVM = QT || SP;
+  static constexpr bool KVM = QT;
   static constexpr int THREADS = NQ * 128 + 32 + 32 * MW;
   static constexpr int WARP_TMA = NQ * 4;
   static constexpr int WARP_MMA = NQ * 4 + 1;  // first MMA warp
@@ -300,11 +291,11 @@ __device__ __forceinline__ bool tagged_add(unsigned long long* w, unsigned tag, 
 // gets a ticket past the last item, then counts itself done, and the last
 // CTA done sets both words to zero, so a replay of the launch from a CUDA
 // graph (same tag) claims them afresh and starts again from ticket 0.
-template <typename T, int D, int NQ, int BN, int NS, bool SP, bool PERS>
-__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
+template <typename T, int D, int NQ, int BN, int NS, bool PERS>
+__global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, PERS>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using C = Cfg<T, D, NQ, BN, NS, SP, PERS>;
+  using C = Cfg<T, D, NQ, BN, NS, PERS>;
   constexpr bool TF32 = Elem<T>::tf32;
   // fp32 items of one key tile, one per CTA (a.v_raw): V arrives row-major in
   // the second stage's value buffer, unused with one key tile, and the TMA
@@ -316,12 +307,12 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;          // [QB]
-  uint64_t* q_empty = q_full + C::QB;  // [QB] Q in shared memory: the item's MMAs are done (one commit per MMA warp)
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + 1;  // Q in shared memory: the item's MMAs are done (one commit per MMA warp)
   // With KVM the key and value tiles of a stage share k_full / k_empty (one
   // wait and one commit per key tile; v_full / v_empty unused); otherwise K
   // and V have their own, so that a key slot frees as soon as QK^T is done.
-  uint64_t* k_full = q_empty + C::QB;
+  uint64_t* k_full = q_empty + 1;
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
@@ -333,11 +324,9 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
   uint64_t* qt_full = mma_done + 1;  // Q copied into tensor memory (one arrive per softmax warp)
   uint64_t* item_full = qt_full + 1;  // ring slot holds the next item (-1: none left)
   uint64_t* item_empty = item_full + C::NR;  // every consumer warp has read the slot
-  uint64_t* s_free = item_empty + C::NR;     // SP: S of tile t read into registers (one arrive per softmax warp)
-  uint64_t* pv_done = s_free + NQ;           // SP: the PV product of tile t completed (P and O free again)
-  // the Q shared tiles (buffer b) may take the next item's load once: the
-  // copy into tensor memory is done (QT), or the item's MMAs have completed
-  auto q_free = [&](int b) -> uint64_t* { return C::QT ? qt_full : &q_empty[b]; };
+  // the Q shared tiles may take the next item's load once: the copy into
+  // tensor memory is done (QT), or the item's MMAs have completed
+  uint64_t* q_free = C::QT ? qt_full : q_empty;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
@@ -347,10 +336,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
 
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
-    for (int b = 0; b < C::QB; ++b) {
-      mbar_init(&q_full[b], 1);
-      mbar_init(&q_empty[b], C::MW);  // one commit per MMA warp
-    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, C::MW);  // one commit per MMA warp
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], C::MW);  // one commit per MMA warp
@@ -362,8 +349,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
       mbar_init(&p_full[t], 4);  // one arrive per softmax warp
       mbar_init(&o_full[t], 1);
       mbar_init(&o_free[t], 4);
-      mbar_init(&s_free[t], 4);
-      mbar_init(&pv_done[t], 1);
     }
     mbar_init(mma_done, C::MW);
     mbar_init(qt_full, 4 * NQ);
@@ -419,9 +404,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
     int last_k[NS], last_v[NS];
 #pragma unroll
     for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
-    int q_last[C::QB];  // per Q buffer: item count of the last Q load issued into it
-#pragma unroll
-    for (int b = 0; b < C::QB; ++b) q_last[b] = -1;
+    int q_last = -1;  // item count of the last Q load issued
     if (lane == 0) {
       const uint64_t pol_q = policy_evict_first();
       // The first item's Q goes out before anything else: after an L2 flush
@@ -438,7 +421,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
               tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
                           (w0.qblk * NQ + t) * kTileM, w0.h, w0.b, pol_q);
           q_pre = true;
-          q_last[0] = 0;
+          q_last = 0;
         }
       }
       const uint64_t pol_kv = policy_evict_last();
@@ -481,15 +464,14 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
         if (q_pre) {
           q_pre = false;  // the first item's Q is already on its way
         } else {
-          // buffer qb last held item na - QB, whose MMAs (or Q copy) must be done
-          const int qb = na % C::QB;
-          if (na >= C::QB && !mbar_wait(q_free(qb), (na / C::QB - 1) & 1, ab, SITE_Q_FULL)) break;
-          mbar_arrive_expect_tx(&q_full[qb], NQ * C::Q_TILE);
+          // the tiles last held item na - 1, whose MMAs (or Q copy) must be done
+          if (na >= 1 && !mbar_wait(q_free, (na - 1) & 1, ab, SITE_Q_FULL)) break;
+          mbar_arrive_expect_tx(q_full, NQ * C::Q_TILE);
           for (int t = 0; t < NQ; ++t)
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_4d(&tm_q, &q_full[qb], smem + C::OFF_Q + (qb * NQ + t) * C::Q_TILE + c * C::Q_CHUNK,
-                          c * C::CW, (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
-          q_last[qb] = na;
+              tma_load_4d(&tm_q, q_full, smem + C::OFF_Q + t * C::Q_TILE + c * C::Q_CHUNK, c * C::CW,
+                          (w.qblk * NQ + t) * kTileM, w.h, w.b, pol_q);
+          q_last = na;
         }
         for (int j = w.jb; j < w.je_all; ++j, ++it) {
           const int s = it % NS, r = it / NS;
@@ -586,8 +568,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
     __syncthreads();  // teardown rendezvous
     if (lane == 0 && *abort_flag) {
       // let the copies still in flight land before the CTA's shared memory goes away
-      for (int b = 0; b < C::QB; ++b)
-        if (q_last[b] >= 0) mbar_wait_teardown(&q_full[b], (q_last[b] / C::QB) & 1);
+      if (q_last >= 0) mbar_wait_teardown(q_full, q_last & 1);
       for (int s = 0; s < NS; ++s) {
         if (last_k[s] >= 0) mbar_wait_teardown(&k_full[s], last_k[s] & 1);
         if (last_v[s] >= 0) mbar_wait_teardown(&v_full[s], last_v[s] & 1);
@@ -622,8 +603,8 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
       const uint64_t dV = C::VT ? sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024)
                                 : sdesc_sw128(smem_u32(smem + C::OFF_V), C::KV_CHUNK, 1024);
       // S_t = Q_t K^T into the S columns of query tile t (K tile at descriptor bK)
-      auto issue_s = [&](int t, uint64_t bK, int qb) {
-        const uint64_t a0 = dQ + (((qb * NQ + t) * C::Q_TILE) >> 4);
+      auto issue_s = [&](int t, uint64_t bK) {
+        const uint64_t a0 = dQ + ((t * C::Q_TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
           const uint32_t off_q = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
@@ -646,7 +627,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
       bool ok = true;
       int taken = -1;
 #pragma unroll 1
-      while (ok && !C::SP) {
+      while (ok) {
         if (!PERS && taken >= 0) break;
         const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, true);
         if (taken < 0) taken = 0;
@@ -663,7 +644,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
           for (int tt = 0; tt < TPW; ++tt) {
             const int t = m + tt * C::MW;
             if (sel(je, t) > w.jb) {
-              issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4), 0);
+              issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4));
               mma_commit(&s_full[t]);
             }
           }
@@ -693,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
               // O_t += P_t V: P from tensor memory; V MN-major (rows = keys), or for
               // TF32 the K-major V^T tile (rows = head dims, 8 keys = 32 bytes a step)
               const uint32_t d_o = tmem + t * C::TILE_COLS + C::O_COL;
-              const uint32_t p_t = tmem + t * C::TILE_COLS + C::P_COL;
+              const uint32_t p_t = tmem + t * C::TILE_COLS;  // P over S
 #pragma unroll
               for (int kk = 0; kk < C::PV_STEPS; ++kk) {
                 const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
@@ -710,7 +691,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
                 tc_fence_after();
               }
               if (elect_one()) {
-                issue_s(t, bK, 0);
+                issue_s(t, bK);
                 mma_commit(&s_full[t]);
               }
               __syncwarp();
@@ -749,94 +730,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
         it += w.je_all - w.jb;
         ++na;
       }
-      if constexpr (C::SP) {
-        // SP: one MMA warp per query tile (t = m).  Per key tile j the warp
-        // issues S(j+1) as soon as the softmax has read S(j) into registers
-        // (s_free), then PV(j) once P(j) is written (p_full): the next
-        // scores are computed while the softmax works on these.  P has
-        // columns of its own; pv_done tells the softmax when P and O are
-        // free again.  Every warp waits for and frees every stage of the
-        // item's key range, so the stage phases stay in step.
-        const int t = m;
-        int sn_ = 0, pn = 0, on = 0;  // S tiles issued, P tiles consumed, outputs done (this tile)
-        while (ok) {
-          if (!PERS && taken >= 0) break;
-          const int idx = taken < 0 ? static_cast<int>(blockIdx.x) : next_item(taken, true);
-          if (taken < 0) taken = 0;
-          if (idx < 0) break;
-          int je[NQ];
-          const Item w = decode_item<NQ, BN>(a, idx, je);
-          if (w.je_all <= w.jb) continue;
-          const int je_t = sel(je, t);
-          const int qb = na % C::QB;
-          ok = wait_all(C::QT ? qt_full : &q_full[qb], C::QT ? (na & 1) : ((na / C::QB) & 1), SITE_Q_FULL) &&
-               wait_all(&k_full[it % NS], (it / NS) & 1, SITE_K_FULL);
-          if (!ok) break;
-          if (je_t > w.jb) {
-            if (sn_ > 0) ok = wait_all(&s_free[t], (sn_ - 1) & 1, SITE_S_FULL);
-            if (!ok) break;
-            tc_fence_after();
-            if (elect_one()) {
-              issue_s(t, dK + (((it % NS) * C::KV_TILE) >> 4), qb);
-              mma_commit(&s_full[t]);
-            }
-            __syncwarp();
-            ++sn_;
-          }
-          for (int j = w.jb; ok && j < w.je_all; ++j) {
-            const int i = it + (j - w.jb);
-            const int s_ = i % NS;
-            const int sn = (i + 1) % NS, rn = (i + 1) / NS;
-            bool k_next = false;
-            if (j < je_t) {
-              if (j + 1 < je_t) {
-                ok = k_next = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
-                if (ok) ok = wait_all(&s_free[t], (sn_ - 1) & 1, SITE_S_FULL);
-                if (!ok) break;
-                tc_fence_after();
-                if (elect_one()) {
-                  issue_s(t, dK + ((sn * C::KV_TILE) >> 4), qb);
-                  mma_commit(&s_full[t]);
-                }
-                __syncwarp();
-                ++sn_;
-              }
-              ok = wait_all(&p_full[t], pn & 1, SITE_P_FULL);
-              if (ok && j == w.jb && on > 0) ok = wait_all(&o_free[t], (on - 1) & 1, SITE_O_FULL);
-              if (!ok) break;
-              tc_fence_after();
-              ++pn;
-              const bool last = j + 1 == je_t;
-              if (elect_one()) {
-                const uint32_t d_o = tmem + t * C::TILE_COLS + C::O_COL;
-                const uint32_t p_t = tmem + t * C::TILE_COLS + C::P_COL;
-                const uint64_t bV = dV + ((s_ * C::KV_TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-                  const uint32_t off = C::VT ? ((kk >> 2) * C::VT_CHUNK + (kk & 3) * 32) >> 4
-                                             : (kk * C::PV_ROWS * 128) >> 4;
-                  mma_ts<TF32>(d_o, p_t + kk * 8, bV + off, idesc_pv, (j > w.jb || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&pv_done[t]);
-                if (last) mma_commit(&o_full[t]);
-              }
-              __syncwarp();
-              if (last) ++on;
-            }
-            if (j + 1 < w.je_all && !k_next) ok = wait_all(&k_full[sn], rn & 1, SITE_K_FULL);
-            if (!ok) break;
-            if (elect_one()) mma_commit(&k_empty[s_]);
-            __syncwarp();
-          }
-          if (!ok) break;
-          if constexpr (!C::QT) {
-            if (elect_one()) mma_commit(&q_empty[qb]);  // this item's MMAs read Q buffer qb
-            __syncwarp();
-          }
-          it += w.je_all - w.jb;
-          ++na;
-        }
-      }
     }
     __syncwarp();
     __syncthreads();  // teardown rendezvous
@@ -859,7 +752,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
     const uint32_t tS = tmem + (static_cast<uint32_t>(wq * 32) << 16) + t * C::TILE_COLS;
     const uint32_t tO = tS + C::O_COL;
     int sc = 0, oc = 0, na = 0;  // S tiles, outputs and Q copies so far (barrier phases)
-    int pvc = 0;                 // P tiles written so far (SP: pv_done phases)
     bool ok = true;
     // Copy this thread's Q row of item idx (TF32-rounded by the load for
     // fp32; packed pairs for bf16/fp16) from the swizzled shared tile into
@@ -918,11 +810,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
         tc_fence_after();
         uint32_t s[BN];
         load_row<BN>(tS, s);
-        if constexpr (C::SP) {  // S is in registers: the next QK^T may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[t]);
-        }
         const int kv0 = j * BN;
         if (kv0 + BN > kv_lim || (a.causal && kv0 + BN - 1 > q_lo + off)) {
           int lim = kv_lim;
@@ -951,22 +838,13 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        if constexpr (C::SP) {
-          // P and O are free once the previous PV of this tile completed
-          // (long since, as a rule: it was issued a whole softmax step ago)
-          if (pvc > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (pvc - 1) & 1, ab, SITE_P_FULL));
-            if (!ok) break;
-            tc_fence_after();
-          }
-        }
         float rsa[8];  // row sum: 8 independent partial sums
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq) rsa[kq] = 0.f;
-        // P by halves of 64 columns.  TF32, and SP: each half is stored to
-        // tensor memory as soon as it is formed (over S, whose values are all
-        // in registers by now, or into P's own columns with SP), formed in
-        // place in s[] (a word goes to a slot already read).  TF32 rounds to
+        // P by halves of 64 columns.  TF32: each half is stored to tensor
+        // memory as soon as it is formed (over S, whose values are all in
+        // registers by now), formed in place in s[] (a word goes to a slot
+        // already read).  TF32 rounds to
         // nearest (ties away) by adding half a TF32 ulp to the bit pattern:
         // the kind::tf32 product reads only the top 19 bits of each 32-bit
         // element, P >= 0 and finite, so a carry into the exponent is the
@@ -986,22 +864,17 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
             if constexpr (TF32) {
               s[c] = f2u(p0) + 0x1000u;
               s[c + 1] = f2u(p1) + 0x1000u;
-            } else if constexpr (C::SP) {
-              s[h + (c - h) / 2] = Elem<T>::pack2(p0, p1);
             } else {
               s[c] = f2u(p0);
               s[c + 1] = f2u(p1);
             }
           }
           if constexpr (TF32) {
-            if (h == 0) tmem_st_x64_at<0>(tS + C::P_COL, s);
-            else tmem_st_x64_at<(BN > 64 ? 64 : 0)>(tS + C::P_COL + 64, s);
-          } else if constexpr (C::SP) {
-            if (h == 0) tmem_st_x32_at<0>(tS + C::P_COL, s);
-            else tmem_st_x32_at<(BN > 64 ? 64 : 0)>(tS + C::P_COL + 32, s);
+            if (h == 0) tmem_st_x64_at<0>(tS, s);
+            else tmem_st_x64_at<(BN > 64 ? 64 : 0)>(tS + 64, s);
           }
         }
-        if constexpr (!TF32 && !C::SP) {
+        if constexpr (!TF32) {
           // half precision over S: packed once the whole row is formed (by
           // halves this form measured spills)
           uint32_t pk[BN / 2];
@@ -1036,7 +909,6 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[t]);
-        ++pvc;
       }
       if (!ok) break;
       // The next item's Q goes into tensor memory before this item's output
@@ -1141,11 +1013,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, SP, PERS>::THREADS, 1)
   }
 }
 
-template <typename T, int D, int NQ, int BN, int NS, bool SP, bool PERS>
+template <typename T, int D, int NQ, int BN, int NS, bool PERS>
 cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& b,
                         int grid, cudaStream_t st) {
-  using C = Cfg<T, D, NQ, BN, NS, SP, PERS>;
-  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, SP, PERS>;
+  using C = Cfg<T, D, NQ, BN, NS, PERS>;
+  auto kern = attn_fwd_kernel<T, D, NQ, BN, NS, PERS>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1162,7 +1034,7 @@ cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 // One CTA per item when the items fit on the SMs at once, or when there are
 // no ticket words (a launch without workspace for them); otherwise the
 // persistent form on every SM, drawing items by ticket.
-template <typename T, int D, int NQ, int BN, int NS, bool SP>
+template <typename T, int D, int NQ, int BN, int NS>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                        int splits, cudaStream_t st) {
   int dev = 0, sms = 0;
@@ -1176,8 +1048,8 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   AttnArgs b = a;
   b.splits = splits;
   if (items <= sms || a.sched == nullptr)
-    return launch_form<T, D, NQ, BN, NS, SP, false>(tq, tk, tv, b, static_cast<int>(items), st);
-  return launch_form<T, D, NQ, BN, NS, SP, true>(tq, tk, tv, b, sms, st);
+    return launch_form<T, D, NQ, BN, NS, false>(tq, tk, tv, b, static_cast<int>(items), st);
+  return launch_form<T, D, NQ, BN, NS, true>(tq, tk, tv, b, sms, st);
 }
 
 }  // namespace
@@ -1200,20 +1072,16 @@ bool attn_shape(la_dtype dt, int D, AttnShape* s) {
 
 cudaError_t launch_attn(la_dtype dt, int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnArgs& a, int splits, cudaStream_t st) {
-  // SP (P in columns of its own, the next QK^T during this softmax) measured
-  // slower everywhere so far: half precision D=64 (bound by its softmax) 4%,
-  // fp32 D=64 on 64-key tiles (the only fp32 tile that leaves room for P)
-  // 37%, its N=64 QK^T products costing more than the overlap saves.
   switch (dt) {
     case LA_BF16:
-      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3, false>(tq, tk, tv, a, splits, st)
-                     : launch_one<__nv_bfloat16, 128, 2, 128, 2, false>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<__nv_bfloat16, 64, 2, 128, 3>(tq, tk, tv, a, splits, st)
+                     : launch_one<__nv_bfloat16, 128, 2, 128, 2>(tq, tk, tv, a, splits, st);
     case LA_F16:
-      return D == 64 ? launch_one<__half, 64, 2, 128, 3, false>(tq, tk, tv, a, splits, st)
-                     : launch_one<__half, 128, 2, 128, 2, false>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<__half, 64, 2, 128, 3>(tq, tk, tv, a, splits, st)
+                     : launch_one<__half, 128, 2, 128, 2>(tq, tk, tv, a, splits, st);
     case LA_F32:
-      return D == 64 ? launch_one<float, 64, 2, 128, 2, false>(tq, tk, tv, a, splits, st)
-                     : launch_one<float, 128, 1, 64, 2, false>(tq, tk, tv, a, splits, st);
+      return D == 64 ? launch_one<float, 64, 2, 128, 2>(tq, tk, tv, a, splits, st)
+                     : launch_one<float, 128, 1, 64, 2>(tq, tk, tv, a, splits, st);
   }
   return cudaErrorInvalidValue;
 }
