@@ -106,8 +106,14 @@ struct Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
   static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes: 4 KB per softmax warp (PERS)
-  static constexpr int OFF_BAR = OFF_STG + (PERS ? NQ * 4 * 4096 : 0);
+  // Epilogue stores: persistent fp32 stores each thread's 256- or 512-byte
+  // row directly (measured 2% faster on fp32 causal S=2048 than through the
+  // boxes); the other persistent forms go through 4 KB store boxes per
+  // softmax warp, so that each store instruction writes whole 128-byte row
+  // segments; the single-item form stages in its dead Q tiles.
+  static constexpr bool DIRECT_O = (E == 4) && PERS;
+  static constexpr int OFF_STG = OFF_V + NS * KV_TILE;  // epilogue store boxes (PERS, not DIRECT_O)
+  static constexpr int OFF_BAR = OFF_STG + (PERS && !DIRECT_O ? NQ * 4 * 4096 : 0);
   // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NQ], p_full[NQ],
   // o_full[NQ], o_free[NQ], mma_done, qt_full, item_full[NR], item_empty[NR]
   static constexpr int NR = 4;  // work items handed from the scheduling thread to the other roles
@@ -245,6 +251,41 @@ __device__ __forceinline__ Item decode_item(const AttnArgs& a, int idx, int (&je
     w.je_all = max(w.je_all, je[t]);
   }
   return w;
+}
+
+// V [BN keys, D] -> V^T [D, BN keys] in shared memory.  The source holds
+// 128-byte rows of CW head dims (chunk c = dims c*CW.., KV_CHUNK bytes), the
+// destination 128-byte rows of CW keys (chunk jc = keys jc*CW.., VT_CHUNK
+// bytes), both in the 128-byte swizzle the tensor copies use (16-byte unit u
+// of row r at u ^ r%8).  By 4x4 blocks (four 16-byte loads, four 16-byte
+// stores): in pass i lane l takes key block 8*(g % NA8) + l%4 + 4*(i & 1) and
+// dim block 8*(g / NA8) + l/4 (g = i / 2), so that every load and store
+// instruction of the warp touches each of the eight 16-byte bank positions
+// exactly four times (no bank conflict).
+template <int D, int BN, int CW, int KV_CHUNK, int VT_CHUNK>
+__device__ __forceinline__ void transpose_v_tile(uint32_t src, uint32_t dst, int lane) {
+  constexpr int NA8 = BN / 32, NB8 = D / 32;
+  static_assert(BN % 32 == 0 && D % 32 == 0, "8x8 groups of 4x4 blocks");
+#pragma unroll 1
+  for (int i = 0; i < 2 * NA8 * NB8; ++i) {
+    const int g = i >> 1;
+    const int k0 = 4 * (8 * (g % NA8) + (lane & 3) + 4 * (i & 1));
+    const int d0 = 4 * (8 * (g / NA8) + (lane >> 2));
+    const int c = d0 / CW, u = (d0 % CW) / 4;
+    uint32_t e[4][4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int rk = k0 + rr;
+      const uint4 x = lds128(src + c * KV_CHUNK + rk * 128 + ((u ^ (rk & 7)) << 4));
+      e[rr][0] = x.x, e[rr][1] = x.y, e[rr][2] = x.z, e[rr][3] = x.w;
+    }
+    const int jc = k0 / CW, u2 = (k0 % CW) / 4;
+#pragma unroll
+    for (int dd = 0; dd < 4; ++dd) {
+      const int d = d0 + dd;
+      sts128(dst + jc * VT_CHUNK + d * 128 + ((u2 ^ (d & 7)) << 4), make_uint4(e[0][dd], e[1][dd], e[2][dd], e[3][dd]));
+    }
+  }
 }
 
 // je[t] for a t not known at compile time, without indexing local memory.
@@ -531,34 +572,11 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, PERS>::THREADS, 1)
     }
     __syncwarp();
     if constexpr (VRAW_OK) {
-      // V [keys, D] (128-byte rows of CW head dims, chunk c = dims c*CW..) into
-      // V^T [D, keys] (128-byte rows of CW keys, chunk jc = keys jc*CW..), both
-      // in the 128-byte swizzle the tensor copies use (16-byte unit u of row r
-      // at u ^ r%8), by 4x4 blocks: four 16-byte loads, four 16-byte stores
+      // the raw tile (second stage's value buffer) into the first stage's V^T tile
       if (vraw && __shfl_sync(0xffffffffu, last_v[1], 0) == 0 &&
           __all_sync(0xffffffffu, mbar_wait(&v_full[1], 0, ab, SITE_V_FULL))) {
-        const uint32_t src = smem_u32(smem + C::OFF_V + C::KV_TILE);
-        const uint32_t dst = smem_u32(smem + C::OFF_V);
-        constexpr int DB = D / 4;  // 4x4 blocks across the head dims
-#pragma unroll 1
-        for (int blk = lane; blk < (BN / 4) * DB; blk += 32) {
-          const int k0 = 4 * (blk / DB), d0 = 4 * (blk % DB);
-          const int c = d0 / C::CW, u = (d0 % C::CW) / 4;
-          uint32_t e[4][4];
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const int r = k0 + rr;
-            const uint4 x = lds128(src + c * C::KV_CHUNK + r * 128 + ((u ^ (r & 7)) << 4));
-            e[rr][0] = x.x, e[rr][1] = x.y, e[rr][2] = x.z, e[rr][3] = x.w;
-          }
-          const int jc = k0 / C::CW, u2 = (k0 % C::CW) / 4;
-#pragma unroll
-          for (int dd = 0; dd < 4; ++dd) {
-            const int d = d0 + dd;
-            sts128(dst + jc * C::VT_CHUNK + d * 128 + ((u2 ^ (d & 7)) << 4),
-                   make_uint4(e[0][dd], e[1][dd], e[2][dd], e[3][dd]));
-          }
-        }
+        transpose_v_tile<D, BN, C::CW, C::KV_CHUNK, C::VT_CHUNK>(smem_u32(smem + C::OFF_V + C::KV_TILE),
+                                                                smem_u32(smem + C::OFF_V), lane);
         fence_proxy_async_smem();  // the PV products read the tile through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&v_full[0]);
@@ -952,6 +970,23 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, PERS>::THREADS, 1)
         if (row_ok && LA_IN_BOUNDS((prow - a.part_o) / D, 1, a.part_elems / D, a.err))
           a.part_lse[(static_cast<size_t>(w.split) * a.B * a.H + w.bh) * a.S_q + q_row] =
               l > 0.f ? m_run + __log2f(l) : -INFINITY;
+      } else if (has_o && C::DIRECT_O) {
+        T* drow = reinterpret_cast<T*>(a.o) + w.b * a.o_sb + w.h * a.o_sh + static_cast<long long>(q_row) * a.o_ss;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c0, o);
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = u2f(o[c]) * inv;
+          if (c0 + 32 >= D) {  // O read out: the next item's PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[t]);
+          }
+          if (row_ok && LA_IN_BOUNDS(drow - reinterpret_cast<T*>(a.o) + c0, 32, a.o_elems, a.err))
+            store_out32<T>(drow + c0, v);
+        }
       } else if (has_o) {
         // Through shared memory, so that each store instruction writes whole
         // 128-byte row segments (four rows of the warp per instruction).

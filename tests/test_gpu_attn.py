@@ -240,3 +240,37 @@ def test_fp32_one_key_tile_transposes_v_in_kernel(D, S_q, S_kv):
     P = oracle.attn_probs(q, k, causal=True)
     assert_within_tf32(halves, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5),
                        f"in-kernel V transpose D={D} S_kv={S_kv}")
+
+
+def _vt_given(q, k, v, causal):
+    """The same attention with V^T handed to the kernel: one window of the
+    chunked mode, whose fp32 cache keeps V transposed."""
+    B, H, S, D = q.shape
+    cache = api.KVCache(B, H, S, D, torch.float32)
+    return api.attn_chunked(q, k, v, cache, causal=causal)
+
+
+@pytest.mark.parametrize("D,S,causal,padded", [(64, 512, True, False), (64, 300, False, True),
+                                               (128, 256, True, False), (128, 200, False, False)])
+def test_fp32_persistent_pre_pass_equals_vt_given(D, S, causal, padded):
+    """fp32 calls in the persistent form (more items than SMs; the epilogue
+    stores each row directly): the V^T pre-pass result equals, bit for bit,
+    the result with V^T handed in (one window of the chunked mode, whose
+    fp32 cache keeps V transposed), and both stay within the TF32 bound of
+    the oracle.  Several key tiles per item, ragged tails, key padding."""
+    B, H = 2, 80
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.float32, seed=141 + D + S)
+    kv_len = torch.tensor([S, S // 2 + 3], dtype=torch.int32) if padded else None
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    kl = kv_len.cuda() if padded else None
+    o = api.attn_fwd(qd, kd, vd, causal=causal, kv_len=kl)
+    assert api.get_last_error() == api.LA_OK
+    if not padded:
+        ref = _vt_given(qd, kd, vd, causal)
+        assert api.get_last_error() == api.LA_OK
+        assert torch.equal(o, ref)
+    kln = kv_len.numpy() if padded else None
+    want = oracle.attn(q, k, v, causal=causal, kv_len=kln)
+    P = oracle.attn_probs(q, k, causal=causal, kv_len=kln)
+    assert_within_tf32(o, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5),
+                       f"persistent fp32 D={D} S={S}")
