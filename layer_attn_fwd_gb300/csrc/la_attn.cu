@@ -17,7 +17,10 @@
 //                          in the persistent form draws the items and hands
 //                          them to the other warps.  For fp32 (TF32
 //                          products, which take K-major operands only) V
-//                          comes from its transpose V^T.
+//                          comes from its transpose V^T; an fp32 item of one
+//                          key tile (one CTA per item) may instead load V
+//                          row-major into the idle second stage, and this
+//                          warp writes it transposed into the first.
 //   warps 4*NQ+1..         tcgen05.mma issuers (one, or one per query tile
 //   (MMA)                  where Q sits in tensor memory):  S_t = Q_t K_j^T
 //                          into tensor memory, then O_t += P_t V_j with P_t
