@@ -157,6 +157,24 @@ class Clocks:
         return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows), "ok": ok}
 
 
+def skip_reason(nbytes, free):
+    """Why a workload needing `nbytes` of device memory is not run with
+    `free` bytes free (10% and 256 MB of headroom), or None when it fits."""
+    if nbytes * 1.1 + (256 << 20) > free:
+        return f"needs about {nbytes / 1e9:.2f} GB on the device, {free / 1e9:.2f} GB free"
+    return None
+
+
+def require_clean(commit):
+    """The --require-clean refusal for a work tree state (`_commit()`'s
+    string, or None outside a git work tree), or None when it may run."""
+    if commit is None:
+        return "--require-clean: not a git work tree"
+    if commit.endswith("+dirty"):
+        return f"--require-clean: tracked files differ from {commit[:-6]}"
+    return None
+
+
 def _commit():
     try:
         r = subprocess.run(["git", "-C", ROOT, "rev-parse", "--short", "HEAD"], capture_output=True, text=True,
@@ -513,9 +531,9 @@ def other_workloads(args, dev, stream, flush, barrier, peaks, cpu_ok=False):
         """Memory pre-check: a workload whose device tensors would not fit in
         the free device memory is recorded as skipped, with the reason,
         instead of being run."""
-        free = torch.cuda.mem_get_info(dev)[0]
-        if nbytes * 1.1 + (256 << 20) > free:
-            res[name] = {"skipped": f"needs about {nbytes / 1e9:.2f} GB on the device, {free / 1e9:.2f} GB free"}
+        why = skip_reason(nbytes, torch.cuda.mem_get_info(dev)[0])
+        if why is not None:
+            res[name] = {"skipped": why}
             return False
         return True
 
@@ -904,10 +922,9 @@ def main():
                          "so that a logged number names the code it measured")
     args = ap.parse_args()
     if args.require_clean:
-        c = _commit()
-        if c is None or c.endswith("+dirty"):
-            print(json.dumps({"error": "--require-clean: " + ("not a git work tree" if c is None
-                                                              else f"tracked files differ from {c[:-6]}")}))
+        why = require_clean(_commit())
+        if why is not None:
+            print(json.dumps({"error": why}))
             sys.exit(2)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")

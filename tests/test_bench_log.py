@@ -47,3 +47,19 @@ def test_log_appends_with_commit(tmp_path, capsys):
     recs = [json.loads(x) for x in open(path)]
     assert [r["value"] for r in recs] == [1.0, 2.0]
     assert all("commit" in r and "logged_at" in r for r in recs)
+
+
+def test_memory_pre_check_records_why_a_workload_is_skipped():
+    """A workload is run only when its device tensors fit in the free memory
+    with 10% and 256 MB of headroom; otherwise the line records why."""
+    GB = 1 << 30
+    assert bench.skip_reason(10 * GB, 100 * GB) is None
+    assert bench.skip_reason(int(100 * GB / 1.1), 100 * GB) is not None  # no room left for the headroom
+    why = bench.skip_reason(300 * GB, 280 * GB)
+    assert why is not None and "322.12 GB" in why and "300.65 GB free" in why
+
+
+def test_require_clean_refuses_a_modified_or_unknown_tree():
+    assert bench.require_clean("ab12cd3") is None
+    assert bench.require_clean("ab12cd3+dirty") == "--require-clean: tracked files differ from ab12cd3"
+    assert bench.require_clean(None) == "--require-clean: not a git work tree"
