@@ -63,3 +63,27 @@ def test_qkv_proj_wide_model(dtype):
     else:
         for got, want, n in ((q, wq, "q"), (k, wk, "k"), (v, wv, "v")):
             assert_close(got, want, dtype, f"qkv_proj {n} d=4096")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=_id)
+def test_long_key_range_one_call(dtype):
+    """256 queries against 500,000 keys in one call (3907 key tiles, split
+    across CTAs and merged by the combine kernel), causal rows aligned to the
+    end with key padding on one head: every output element.  The values
+    carry a ramp over key positions (0 to 4), so that every output depends
+    on which keys were included: a split left out or counted twice moves it
+    far beyond the tolerance."""
+    B, H, S_q, S_kv, D = 2, 1, 256, 500_000, 64
+    q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, dtype, seed=73)
+    ramp = 4.0 * torch.arange(S_kv, dtype=torch.float32) / S_kv
+    v = (v.float() + ramp[None, None, :, None]).to(dtype)
+    kv_len = torch.tensor([S_kv, 333_333], dtype=torch.int32)
+    o = api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, kv_len=kv_len.cuda())
+    assert api.get_last_error() == api.LA_OK
+    want = oracle.attn(q, k, v, causal=True, kv_len=kv_len.numpy())
+    if dtype == torch.float32:
+        P = oracle.attn_probs(q, k, causal=True, kv_len=kv_len.numpy())
+        bound = tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5)
+        assert_within_tf32(o, want, bound, "S_kv = 500000")
+    else:
+        assert_close(o, want, dtype, "S_kv = 500000")
