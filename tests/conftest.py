@@ -12,7 +12,7 @@ def pytest_configure(config):
 
 def pytest_terminal_summary(terminalreporter):
     """fp32 parity held to the TF32 bound: how many elements of each case lie
-    beyond the spec pair atol 1e-3 / rtol 1e-2."""
+    beyond the fp32 tolerance pair atol 1e-3 / rtol 1e-2."""
     try:
         from gpu_util import TF32_RECORDS
     except Exception:
@@ -21,4 +21,4 @@ def pytest_terminal_summary(terminalreporter):
         return
     terminalreporter.write_sep("-", "fp32 (TF32) parity: elements beyond atol 1e-3 / rtol 1e-2, all within the TF32 bound")
     for what, beyond, n, worst in TF32_RECORDS:
-        terminalreporter.write_line(f"{what}: {beyond} of {n} beyond the north-star pair; worst err/bound {worst:.3f}")
+        terminalreporter.write_line(f"{what}: {beyond} of {n} beyond atol 1e-3 / rtol 1e-2; worst err/bound {worst:.3f}")

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import tf32_bound as tb
-from gpu_util import TOL, assert_close, assert_within_tf32, need_gpu
+from gpu_util import TOL, assert_close, assert_within_tf32, need_gpu, with_ramp
 from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
@@ -198,6 +198,17 @@ def test_workload_bf16_causal_4096_every_row():
     q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=35)
     o = _gpu_attn(q, k, v, True).cpu()
     assert_close(o, oracle.attn(q, k, v, causal=True), torch.bfloat16, "bf16 causal 4096 every row")
+
+
+def test_workload_bf16_causal_4096_ramp_values_every_row():
+    """The bf16 workload with a ramp over key positions added to the values
+    (gpu_util.with_ramp), so that a key tile left out or counted twice fails
+    the tolerance: every output element."""
+    B, H, S, D = 4, 16, 4096, 128
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=36)
+    v = with_ramp(v)
+    o = _gpu_attn(q, k, v, True).cpu()
+    assert_close(o, oracle.attn(q, k, v, causal=True), torch.bfloat16, "bf16 causal 4096 ramp values")
 
 
 @pytest.mark.parametrize("seed", range(2))

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, need_gpu
+from gpu_util import assert_close, need_gpu, with_ramp
 from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
@@ -87,3 +87,18 @@ def test_chunked_100k_sampled_rows():
     want = oracle.attn_rows(q, k, v, rows, causal=True)
     r = rows.numpy()
     assert_close(o[r[:, 0], r[:, 1], r[:, 2]], want, torch.bfloat16, "100k sampled rows")
+
+
+def test_chunked_100k_ramp_values_sampled_rows():
+    """The 100k-token chunked run with a ramp over key positions added to the
+    values (gpu_util.with_ramp): a window that missed part of the cache, or
+    saw a key twice, moves its rows far beyond the tolerance.  256 seeded
+    rows including the window boundaries and the last row."""
+    B, H, S, D, C = 2, 16, 100000, 64, 4096
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, torch.bfloat16, seed=62)
+    v = with_ramp(v)
+    o = _run_chunked(q.cuda(), k.cuda(), v.cuda(), C).cpu()
+    rows = inputs.sample_rows(B, H, S, n=256, seed=1235, forced=(0, 4095, 4096, 98303, 98304, 99999))
+    want = oracle.attn_rows(q, k, v, rows, causal=True)
+    r = rows.numpy()
+    assert_close(o[r[:, 0], r[:, 1], r[:, 2]], want, torch.bfloat16, "100k sampled rows, ramp values")

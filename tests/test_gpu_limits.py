@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import tf32_bound as tb
-from gpu_util import assert_close, assert_within_tf32, need_gpu
+from gpu_util import assert_close, assert_within_tf32, need_gpu, with_ramp
 from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
@@ -75,8 +75,7 @@ def test_long_key_range_one_call(dtype):
     far beyond the tolerance."""
     B, H, S_q, S_kv, D = 2, 1, 256, 500_000, 64
     q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, dtype, seed=73)
-    ramp = 4.0 * torch.arange(S_kv, dtype=torch.float32) / S_kv
-    v = (v.float() + ramp[None, None, :, None]).to(dtype)
+    v = with_ramp(v, 4.0)
     kv_len = torch.tensor([S_kv, 333_333], dtype=torch.int32)
     o = api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, kv_len=kv_len.cuda())
     assert api.get_last_error() == api.LA_OK
