@@ -144,7 +144,19 @@ struct Cfg {
   // in tensor memory (fp32 D=64 +3%, bf16 D=64 +7%); bf16 D=128 with its
   // two 64 KB stages needs the key slot back before PV is done (-7%).
   static constexpr bool KVM = QT;
-  static constexpr int THREADS = NQ * 128 + 32 + 32 * MW;
+  // Register split (SMR): the block of more than 256 threads is launched at
+  // 168 registers a thread; the softmax warpgroups then take R_SOFT and the
+  // TMA and MMA warps (with a padding warp, so that they fill a warpgroup)
+  // give back to R_REST: 256 x 184 + 128 x 120 = 62464 <= 384 x 168.
+  // Measured for half precision D=64 (window B2 H16 S_q4096 S_kv40960
+  // 1375 against 1399 us, causal S=4096 133 against 138 us); fp32 D=64 and
+  // half precision D=128 measured 1% slower with it, and a larger softmax
+  // share spills in the MMA and TMA warps.
+  static constexpr bool SMR = (E == 2) && (D == 64) && (NQ == 2);
+  static constexpr int R_SOFT = 184, R_REST = 120;
+  static constexpr int THREADS_USED = NQ * 128 + 32 + 32 * MW;
+  static constexpr int THREADS = SMR ? (THREADS_USED + 127) / 128 * 128 : THREADS_USED;
+  static_assert(!SMR || NQ * 128 * R_SOFT + (THREADS - NQ * 128) * R_REST <= THREADS * 168, "register split");
   static constexpr int WARP_TMA = NQ * 4;
   static constexpr int WARP_MMA = NQ * 4 + 1;  // first MMA warp
   static_assert(D % CW == 0, "head dim must fill whole 128-byte rows");
@@ -445,6 +457,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, PERS>::THREADS, 1)
 
   if (warp == C::WARP_TMA) {
     // ======================= TMA producer ==================================
+    if constexpr (C::SMR) setmaxnreg_dec<C::R_REST>();
     int last_k[NS], last_v[NS];
 #pragma unroll
     for (int s = 0; s < NS; ++s) last_k[s] = last_v[s] = -1;
@@ -596,8 +609,14 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, PERS>::THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp >= C::WARP_MMA + C::MW) {
+    // padding warp of the register split: gives its registers back and
+    // joins the teardown rendezvous
+    if constexpr (C::SMR) setmaxnreg_dec<C::R_REST>();
+    __syncthreads();
   } else if (warp >= C::WARP_MMA) {
     // ======================= MMA issuers ===================================
+    if constexpr (C::SMR) setmaxnreg_dec<C::R_REST>();
     // MMA warp m issues for query tiles t = m, m + MW, ...  Step j issues
     // PV(j) and S(j+1).  With KVM, V(j) arrived with K(j) (waited for before
     // S(j)), stage j+1 is waited for before S(j+1), and stage j is freed at
@@ -767,6 +786,7 @@ __global__ void __launch_bounds__(Cfg<T, D, NQ, BN, NS, PERS>::THREADS, 1)
     }
   } else {
     // ======================= softmax of query tile t ========================
+    if constexpr (C::SMR) setmaxnreg_inc<C::R_SOFT>();
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
@@ -1064,6 +1084,15 @@ cudaError_t launch_form(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    if constexpr (C::SMR) {
+      // the register split must fit in what the block is launched with
+      // (otherwise the softmax warps' increase would never be granted)
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs * C::THREADS < NQ * 128 * C::R_SOFT + (C::THREADS - NQ * 128) * C::R_REST)
+        return cudaErrorInvalidConfiguration;
+    }
     configured[dev] = true;
   }
   return launch_pdl("attn_fwd_kernel", kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, tq, tk, tv, b);

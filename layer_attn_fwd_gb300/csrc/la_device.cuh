@@ -261,6 +261,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // warp-uniform; measured on GB300, an MMA loop run by one lane alone (inside
 // `if (lane == 0)`) issued a step of 12 MMAs in ~1030 cycles against ~650
 // for the same loop on the whole warp with an elected issuer.
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute the same one): give registers back down to N a thread, or wait
+// until the block has N a thread to grant.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(
