@@ -71,21 +71,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   }
 }
 
-// blockIdx.y selects k (0) or v (1); a keys-only launch has one row of blocks.
+// blockIdx.z selects k (0) or v (1) (a keys-only launch has one), blockIdx.y
+// the (b, h) pair.  A pair's new rows are one contiguous run of per_head
+// 16-byte vectors in the source and in the cache (rows at.. of its [S_max, D]
+// block), so the copy needs no index arithmetic beyond the two bases; each
+// thread keeps four 16-byte loads in flight.
 __global__ void __launch_bounds__(256)
     kv_append_kernel(const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint8_t* k_dst,
-                     uint8_t* v_dst, long long n_vec, int vec_per_row, int rows, long long dst_head_bytes,
-                     long long at_bytes) {
-  const uint4* src = blockIdx.y == 0 ? k_src : v_src;
-  uint8_t* dst = blockIdx.y == 0 ? k_dst : v_dst;
-  const long long row_bytes = static_cast<long long>(vec_per_row) * 16;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < n_vec;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = g / vec_per_row;  // row over all (b, h)
-    const long long c = g - r * vec_per_row;
-    const long long bh = r / rows;
-    const long long rr = r - bh * rows;
-    *reinterpret_cast<uint4*>(dst + bh * dst_head_bytes + at_bytes + rr * row_bytes + c * 16) = src[g];
+                     uint8_t* v_dst, int per_head, long long dst_head_bytes, long long at_bytes) {
+  const uint4* src = (blockIdx.z == 0 ? k_src : v_src) + static_cast<long long>(blockIdx.y) * per_head;
+  uint4* dst = reinterpret_cast<uint4*>((blockIdx.z == 0 ? k_dst : v_dst) + blockIdx.y * dst_head_bytes + at_bytes);
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < per_head; i += 4 * step) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * step < per_head) w[u] = src[i + u * step];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * step < per_head) dst[i + u * step] = w[u];
   }
 }
 
@@ -407,15 +411,20 @@ cudaError_t launch_layernorm(la_dtype dt, const void* x, const void* gamma, cons
 cudaError_t launch_kv_append(const void* k_src, const void* v_src, void* k_dst, void* v_dst, int B, int H,
                              int rows, int D, int S_max, int at, int elem_bytes, cudaStream_t st) {
   const int vec_per_row = D * elem_bytes / 16;
-  const long long n_vec = static_cast<long long>(B) * H * rows * vec_per_row;
-  if (n_vec == 0) return cudaSuccess;
-  const long long want = (n_vec + 255) / 256;
-  const int cap = sm_count() * 4;
-  dim3 grid(static_cast<unsigned>(want < cap ? want : cap), v_src != nullptr ? 2 : 1);  // keys only without v
+  const long long per_head = static_cast<long long>(rows) * vec_per_row;
+  const long long pairs = static_cast<long long>(B) * H;
+  if (per_head == 0 || pairs == 0) return cudaSuccess;
+  if (per_head > 0x7fffffffLL || pairs > 65535) return cudaErrorInvalidValue;
+  // enough blocks per pair for about four waves of the whole grid, each
+  // thread moving four vectors a pass
+  const long long per_pair_want = (per_head + 1023) / 1024;
+  const long long cap = (static_cast<long long>(sm_count()) * 32 + pairs - 1) / pairs;
+  const long long bx = per_pair_want < cap ? per_pair_want : (cap > 0 ? cap : 1);
+  dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(pairs), v_src != nullptr ? 2 : 1);  // keys only without v
   const long long row_bytes = static_cast<long long>(D) * elem_bytes;
   return launch("kv_append_kernel", kv_append_kernel, grid, dim3(256), 0, st, false,
                 reinterpret_cast<const uint4*>(k_src), reinterpret_cast<const uint4*>(v_src),
-                reinterpret_cast<uint8_t*>(k_dst), reinterpret_cast<uint8_t*>(v_dst), n_vec, vec_per_row, rows,
+                reinterpret_cast<uint8_t*>(k_dst), reinterpret_cast<uint8_t*>(v_dst), static_cast<int>(per_head),
                 static_cast<long long>(S_max) * row_bytes, static_cast<long long>(at) * row_bytes);
 }
 
