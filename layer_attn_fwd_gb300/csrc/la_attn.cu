@@ -36,6 +36,10 @@
 //                          memory, so that QK^T reads only K from shared
 //                          memory.
 //
+// Half precision D=64 adds a padding warp, so that the TMA and MMA warps
+// fill a warpgroup of their own, and moves registers from that warpgroup to
+// the softmax warpgroups (setmaxnreg; Cfg::SMR).
+//
 // The two query tiles ping-pong: while tile 0's softmax runs, the tensor core
 // computes PV and the next QK^T of tile 1, and vice versa.  Per tile the MMA
 // issue order is PV_t(j) before S_t(j+1), so when the softmax sees S_t(j+1)
