@@ -102,3 +102,32 @@ def test_chunked_100k_ramp_values_sampled_rows():
     want = oracle.attn_rows(q, k, v, rows, causal=True)
     r = rows.numpy()
     assert_close(o[r[:, 0], r[:, 1], r[:, 2]], want, torch.bfloat16, "100k sampled rows, ramp values")
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float16, 128), (torch.float32, 64)],
+                         ids=lambda p: _id(p) if not isinstance(p, int) else str(p))
+def test_cache_holds_exactly_the_appended_rows(dtype, D):
+    """After windows of uneven length (the last one ragged) the cache holds
+    every appended key row, bit for bit, at its position for every (batch,
+    head) pair, V likewise (fp32: transposed), and the rows past the
+    cache's length keep what was there before (a sentinel)."""
+    B, H, S, S_max = 3, 5, 700, 760
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, dtype, seed=63)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    cache = api.KVCache(B, H, S_max, D, dtype)
+    cache.k.fill_(7.0)
+    cache.v.fill_(7.0)
+    for s0, L in ((0, 256), (256, 1), (257, 300), (557, 143)):
+        sl = slice(s0, s0 + L)
+        api.attn_chunked(qd[:, :, sl].contiguous(), kd[:, :, sl].contiguous(), vd[:, :, sl].contiguous(), cache)
+        assert cache.len == s0 + L
+    assert api.get_last_error() == api.LA_OK
+    ck, cv = cache.k.cpu(), cache.v.cpu()
+    assert torch.equal(ck[:, :, :S], k)
+    assert bool((ck[:, :, S:] == 7.0).all())
+    if dtype == torch.float32:
+        assert torch.equal(cv[:, :, :, :S], v.transpose(2, 3))
+        assert bool((cv[:, :, :, S:] == 7.0).all())
+    else:
+        assert torch.equal(cv[:, :, :S], v)
+        assert bool((cv[:, :, S:] == 7.0).all())
