@@ -1,0 +1,52 @@
+"""A seeded sweep of random attention problems on the GPU through the C ABI,
+element by element against the fp64 oracle: element type, head size, batch,
+heads, query and key lengths (1 to 900, ragged), causal or not, with or
+without key padding (lengths from 0 to past the end).  The sizes span the
+one-CTA-per-item and the persistent forms and split key ranges."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tf32_bound as tb
+from gpu_util import assert_close, assert_within_tf32, need_gpu
+from layer_attn_fwd_gb300 import api, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    need_gpu()
+    build.build()
+    api.load()
+
+
+def _case(seed):
+    r = np.random.default_rng(1000 + seed)
+    dtype = [torch.float32, torch.bfloat16, torch.float16][int(r.integers(3))]
+    D = int(r.choice([64, 128]))
+    B = int(r.integers(1, 5))
+    # fp32 is held to its TF32 bound, which needs the probabilities: fewer heads
+    H = int(r.integers(1, 7 if dtype == torch.float32 else 49))
+    S_q, S_kv = int(r.integers(1, 701)), int(r.integers(1, 901))
+    causal = bool(r.integers(2))
+    kv_len = torch.tensor(r.integers(0, S_kv + 50, size=B), dtype=torch.int32) if r.integers(3) == 0 else None
+    return dtype, D, B, H, S_q, S_kv, causal, kv_len
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_problem(seed):
+    dtype, D, B, H, S_q, S_kv, causal, kv_len = _case(seed)
+    what = f"seed {seed}: {dtype} D={D} B={B} H={H} S_q={S_q} S_kv={S_kv} causal={causal} kv_len={kv_len}"
+    q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, dtype, seed=2000 + seed)
+    kl = kv_len.cuda() if kv_len is not None else None
+    o = api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, kv_len=kl)
+    assert api.get_last_error() == api.LA_OK, what
+    kn = kv_len.numpy() if kv_len is not None else None
+    want = oracle.attn(q, k, v, causal=causal, kv_len=kn)
+    if dtype == torch.float32:
+        P = oracle.attn_probs(q, k, causal=causal, kv_len=kn)
+        assert_within_tf32(o, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5), what)
+    else:
+        assert_close(o, want, dtype, what)
