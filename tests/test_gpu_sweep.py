@@ -50,3 +50,42 @@ def test_random_problem(seed):
         assert_within_tf32(o, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5), what)
     else:
         assert_close(o, want, dtype, what)
+
+
+def _layer_case(seed):
+    r = np.random.default_rng(3000 + seed)
+    dtype = [torch.float32, torch.bfloat16, torch.float16][int(r.integers(3))]
+    D = int(r.choice([64, 128]))
+    H = int(r.integers(1, (512 if dtype == torch.float32 else 1024) // D + 1))
+    B, S = int(r.integers(1, 5)), int(r.integers(1, 601))
+    causal = bool(r.integers(2))
+    kv_len = torch.tensor(r.integers(0, S + 20, size=B), dtype=torch.int32) if r.integers(3) == 0 else None
+    if dtype == torch.float32:
+        # fp32 against the atol/rtol pair: rows that see many keys, where the
+        # TF32 roundings average out (rows of few keys are held to the
+        # element-wise TF32 bound by the attention tests)
+        S, causal, kv_len = max(S, 64), False, None
+    bias = "normal" if r.integers(2) else "zero"
+    prepared = bool(r.integers(2))
+    return dtype, D, H, B, S, causal, kv_len, bias, prepared
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_sublayer(seed):
+    """The projection and attention sublayer on random shapes (d_model = H x D
+    up to 512 for fp32, 1024 for half precision), on per-call or prepared
+    weights, every output element against the fp64 oracle (fp32: non-causal,
+    at least 64 keys a row, see _layer_case)."""
+    dtype, D, H, B, S, causal, kv_len, bias, prepared = _layer_case(seed)
+    dm = H * D
+    what = f"seed {seed}: {dtype} B={B} S={S} d={dm} H={H} causal={causal} kv_len={kv_len} bias={bias} prepared={prepared}"
+    x, W, b = inputs.layer_inputs(B, S, dm, dtype, seed=4000 + seed, bias=bias)
+    xd, Wd, bd = x.cuda(), W.cuda(), b.cuda()
+    kl = kv_len.cuda() if kv_len is not None else None
+    if prepared:
+        o = api.layer_attn_prepared(xd, api.prepare_weight(Wd), bd, H, causal=causal, kv_len=kl)
+    else:
+        o = api.layer_attn(xd, Wd, bd, H, causal=causal, kv_len=kl)
+    assert api.get_last_error() == api.LA_OK, what
+    kn = kv_len.numpy() if kv_len is not None else None
+    assert_close(o, oracle.layer_attn(x, W, b, H, causal=causal, kv_len=kn), dtype, what)
