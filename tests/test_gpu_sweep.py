@@ -89,3 +89,41 @@ def test_random_sublayer(seed):
         assert_within_tf32(o, want, tb.sublayer_bound(x, W, b, H, causal=causal, kv_len=kn), what)
     else:
         assert_close(o, want, dtype, what)
+
+
+def _chunked_case(seed):
+    r = np.random.default_rng(5000 + seed)
+    dtype = [torch.float32, torch.bfloat16, torch.float16][int(r.integers(3))]
+    D = int(r.choice([64, 128]))
+    B, H, S = int(r.integers(1, 4)), int(r.integers(1, 17)), int(r.integers(1, 1501))
+    chunk = int(r.integers(max(1, S // 100), 701))
+    # fp32 is held to the TF32 bound of causal attention over the whole
+    # sequence, which the windows reproduce only when causal
+    causal = True if dtype == torch.float32 else bool(r.integers(2))
+    return dtype, D, B, H, S, chunk, causal
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_chunked(seed):
+    """The chunked mode on random shapes and window lengths (the last window
+    ragged), causal or not, every output element against the window-by-window
+    fp64 oracle; the cache holds the appended keys bit for bit."""
+    dtype, D, B, H, S, chunk, causal = _chunked_case(seed)
+    what = f"seed {seed}: {dtype} D={D} B={B} H={H} S={S} chunk={chunk} causal={causal}"
+    q, k, v = inputs.attn_inputs(B, H, S, S, D, dtype, seed=6000 + seed)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    cache = api.KVCache(B, H, S, D, dtype)
+    outs = []
+    for s0, L in inputs.chunk_bounds(S, chunk):
+        sl = slice(s0, s0 + L)
+        outs.append(api.attn_chunked(qd[:, :, sl].contiguous(), kd[:, :, sl].contiguous(),
+                                     vd[:, :, sl].contiguous(), cache, causal=causal))
+    assert api.get_last_error() == api.LA_OK, what
+    o = torch.cat(outs, dim=2)
+    assert torch.equal(cache.k[:, :, :S].cpu(), k), what
+    want = oracle.attn_chunked(q, k, v, chunk, causal=causal)
+    if dtype == torch.float32:
+        P = oracle.attn_probs(q, k, causal=True)
+        assert_within_tf32(o, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5), what)
+    else:
+        assert_close(o, want, dtype, what)
