@@ -127,3 +127,45 @@ def test_random_chunked(seed):
         assert_within_tf32(o, want, tb.attn_bound(q.numpy(), k.numpy(), v.numpy(), P, want, D ** -0.5), what)
     else:
         assert_close(o, want, dtype, what)
+
+
+def _block_case(seed):
+    r = np.random.default_rng(7000 + seed)
+    dtype = [torch.float32, torch.bfloat16, torch.float16][int(r.integers(3))]
+    D = int(r.choice([64, 128]))
+    H = int(r.integers(1, 768 // D + 1))
+    B, S = int(r.integers(1, 4)), int(r.integers(1, 401))
+    causal = bool(r.integers(2))
+    kv_len = torch.tensor(r.integers(0, S + 20, size=B), dtype=torch.int32) if r.integers(3) == 0 else None
+    prepared = bool(r.integers(2))
+    return dtype, D, H, B, S, causal, kv_len, prepared
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_prenorm_block(seed):
+    """The pre-norm block (LayerNorm fused into the projection, attention,
+    output projection) on random shapes, on per-call or prepared weights,
+    every output element against the fp64 oracle (fp32 held to the composed
+    TF32 bound of the LayerNorm and the three contractions)."""
+    dtype, D, H, B, S, causal, kv_len, prepared = _block_case(seed)
+    dm = H * D
+    what = f"seed {seed}: {dtype} B={B} S={S} d={dm} H={H} causal={causal} kv_len={kv_len} prepared={prepared}"
+    x, W, b = inputs.layer_inputs(B, S, dm, dtype, seed=8000 + seed, bias="normal")
+    gam, bet = inputs.ln_inputs(dm, dtype, seed=8100 + seed)
+    Wo, bo = inputs.out_proj_inputs(dm, dtype, seed=8200 + seed, bias="normal")
+    dev = [t.cuda() for t in (x, gam, bet, W, b, Wo, bo)]
+    kl = kv_len.cuda() if kv_len is not None else None
+    if prepared:
+        y = api.layer_attn_prepared(dev[0], api.prepare_weight(dev[3]), dev[4], H, gamma=dev[1], beta=dev[2],
+                                    Wo_p=api.prepare_weight(dev[5]), bo=dev[6], causal=causal, kv_len=kl)
+    else:
+        y = api.layer_attn_ln(dev[0], dev[1], dev[2], dev[3], dev[4], dev[5], dev[6], H, causal=causal, kv_len=kl)
+    assert api.get_last_error() == api.LA_OK, what
+    kn = kv_len.numpy() if kv_len is not None else None
+    want = oracle.layer_attn_ln(x, gam, bet, W, b, Wo, bo, H, causal=causal, kv_len=kn)
+    if dtype == torch.float32:
+        xhat = oracle.layernorm(x, gam, bet)
+        bound = tb.sublayer_bound(xhat, W, b, H, causal=causal, kv_len=kn, Wo=Wo, bo=bo, dx=tb.layernorm_error(xhat))
+        assert_within_tf32(y, want, bound, what)
+    else:
+        assert_close(y, want, dtype, what)
