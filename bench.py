@@ -67,10 +67,13 @@ def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
-                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+        out = {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+               "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
     except Exception:
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+        out = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    # the nominal figures, for context beside the measured denominators
+    out["nominal"] = {"bf16_tflops": 2250.0, "tf32_tflops": 1100.0, "hbm_gbs": 7900.0}
+    return out
 
 
 def _tensor_peak(dtype, peaks, sustained=False):
@@ -350,11 +353,16 @@ def run_ours(args):
     # ---- each kernel of the step alone (events around every launch) -----------
     kt = kernel_times(api, layer_step, K, flush, stream)
     kernel_flops = {"qkv_proj_kernel": fl_proj, "attn_fwd_kernel": fl_attn}
+    # algorithmic bytes of each stage (fp32): the projection reads x and
+    # Wqkv^T and writes q, k, V^T; the attention reads those and writes o
+    act = B * S * dm * 4
+    kernel_bytes = {"qkv_proj_kernel": act + 3 * dm * dm * 4 + 3 * act, "attn_fwd_kernel": 3 * act + act}
     per_kernel = {}
     for name, t in kt.items():
         e = {"ms": round(t["ms"], 5), "launches_per_step": t["launches_per_step"]}
         if name in kernel_flops:
             e["tflops"] = round(kernel_flops[name] / (t["ms"] * 1e-3) / 1e12, 2)
+            e["gbs"] = round(kernel_bytes[name] / (t["ms"] * 1e-3) / 1e9, 1)
         elif name == "transpose32_kernel":  # Wqkv^T, 3 d^2 fp32 read and written
             e["gbs"] = round(2 * 3 * dm * dm * 4 / (t["ms"] * 1e-3) / 1e9, 1)
         per_kernel[name] = e
