@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -141,6 +142,10 @@ struct Plan {
   int tiles_per_split = 1;
   size_t ws_bytes = 0;  // partials the plan needs
 };
+
+// Bytes of keys and values the concurrently running causal items share
+// (a quarter of the 126 MB of L2, which the two dies split between them).
+constexpr long long kGroupBytes = 32LL << 20;
 
 // The persistent attention's ticket word and done word (two 64-bit words,
 // padded so that what follows stays 256-byte aligned).
@@ -310,6 +315,15 @@ la_status run_attention(const void* q, const KVView& kv, void* o, long long o_sb
   a.sl2 = scale * 1.4426950408889634f;
   a.num_qblk = p.num_qblk;
   a.tiles_per_split = p.tiles_per_split;
+  {
+    // Causal items go out heaviest first within groups of (b, h) pairs whose
+    // keys and values together fill about a quarter of L2, so that the items
+    // that read the same keys run at about the same time and find them there.
+    const long long pair_bytes =
+        std::max(1LL, static_cast<long long>(S_kv) * D * static_cast<long long>(elem_bytes(dt)) * 2);
+    const long long g = std::min(static_cast<long long>(B) * H, kGroupBytes / pair_bytes);
+    a.head_group = static_cast<int>(std::max(1LL, g));
+  }
   a.err = err;
   a.sched = sched;
   a.sched_gen = next_sched_tag();

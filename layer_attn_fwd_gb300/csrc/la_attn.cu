@@ -225,22 +225,30 @@ struct Item {
   int qblk, b, h, bh, split, kv_lim, jb, je_all;
 };
 
-// Causal items are numbered with the query block outermost, the heaviest
-// block (last rows) first, so that handing them out in order is a
-// longest-first schedule.  Non-causal items all weigh the same: they are
-// numbered head by head, so that the query blocks of a head (which read the
-// same keys and values) run side by side.  Key-range splits are innermost.
+// Causal items are numbered by groups of a.head_group (b, h) pairs, and
+// within a group with the query block outermost, the heaviest block (last
+// rows) first: handing them out in order is a longest-first schedule whose
+// last items are light, while the items running at once read the keys and
+// values of a few groups only, which stay in L2.  Non-causal items all weigh
+// the same: they are numbered head by head, so that the query blocks of a
+// head (which read the same keys and values) run side by side.  Key-range
+// splits are innermost.
 // je[t] is one past the last key tile of query tile t (jb when it has none).
 template <int NQ, int BN>
 __device__ __forceinline__ Item decode_item(const AttnArgs& a, int idx, int (&je)[NQ]) {
   Item w;
   int qi;
   if (a.causal) {
-    const int per_q = a.B * a.H * a.splits;
-    qi = idx / per_q;
-    const int rem = idx - qi * per_q;
-    w.bh = rem / a.splits;
-    w.split = rem - w.bh * a.splits;
+    const int per_grp = a.head_group * a.num_qblk * a.splits;
+    const int g = idx / per_grp;
+    const int bh0 = g * a.head_group;
+    const int per_q = min(a.head_group, a.B * a.H - bh0) * a.splits;  // the last group may be short
+    const int rem0 = idx - g * per_grp;
+    qi = rem0 / per_q;
+    const int rem = rem0 - qi * per_q;
+    const int pair = rem / a.splits;
+    w.bh = bh0 + pair;
+    w.split = rem - pair * a.splits;
   } else {
     const int per_bh = a.num_qblk * a.splits;
     w.bh = idx / per_bh;

@@ -69,6 +69,7 @@ struct AttnArgs {
   int num_qblk;               // query blocks (of rows_per_cta rows) per (b, h)
   int tiles_per_split;        // key tiles handled by one split
   int splits;                 // key-range splits (set by the launcher)
+  int head_group;             // causal order: (b, h) pairs per group (>= 1; B*H = one group)
   unsigned long long* sched;  // persistent form: ticket word and done word, in the caller's workspace
   unsigned sched_gen;         // this launch's tag in the high half of both words (never 0)
   uint32_t* err;              // device error word

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import tf32_bound as tb
-from gpu_util import assert_close, assert_within_tf32, need_gpu
+from gpu_util import assert_close, assert_within_tf32, need_gpu, with_ramp
 from layer_attn_fwd_gb300 import api, build, inputs
 
 pytestmark = pytest.mark.gpu
@@ -152,3 +152,25 @@ def test_two_streams_at_once(dtype, D):
             assert_within_tf32(outs[i][0], want, tb.attn_bound(q, k, v, P, want, D ** -0.5), f"two streams {i}")
         else:
             assert_close(outs[i][0], want, dtype, f"stream {i}")
+
+
+@pytest.mark.parametrize("D,S_kv", [(64, 50_000), (128, 24_000)], ids=["D64", "D128"])
+def test_causal_items_in_head_groups(D, S_kv):
+    """Causal items are numbered by groups of (b, h) pairs whose keys and
+    values fill about 32 MB, heaviest first within a group.  bf16 B=1 H=11
+    S_q=4096 with S_kv keys of 12.8 / 12.3 MB a pair: groups of two pairs,
+    the last one short, 176 or more items in the persistent form.  Values
+    carry a ramp over key positions, so an item run twice, skipped or given
+    another head's keys moves its rows far beyond the tolerance.  Every head's
+    first and last rows of each of several query blocks, and 179 seeded rows."""
+    B, H, S_q = 1, 11, 4096
+    assert (32 << 20) // (S_kv * D * 2 * 2) == 2  # pairs per group
+    assert _items(B, H, S_q, torch.bfloat16, D) > SMS
+    q, k, v = inputs.attn_inputs(B, H, S_q, S_kv, D, torch.bfloat16, seed=47 + D)
+    v = with_ramp(v, 4.0)
+    o = _run(q, k, v, causal=True).cpu()
+    edges = [(0, h, i) for h in range(H) for i in (0, 255, 256, 2047, 2048, 3840, 4095)]
+    rows = torch.cat([torch.tensor(edges, dtype=torch.int64), inputs.sample_rows(B, H, S_q, n=179, seed=1240 + D)])
+    want = oracle.attn_rows(q, k, v, rows, causal=True)
+    r = rows.numpy()
+    assert_close(o[r[:, 0], r[:, 1], r[:, 2]], want, torch.bfloat16, f"head groups D={D}")
